@@ -1,0 +1,228 @@
+/*
+ * w4a16_moe.h -- C ABI of the GB300 (sm_103a) W4A16 mixture-of-experts expert path.
+ *
+ * The operation is the indexed W4A16 MoE expert GEMM described on
+ * "vLLM x Novita AI: Chord, Faster INT4 MoE for Kimi K2.x": BF16 activations,
+ * uint4 weights with one BF16 scale per 32 consecutive K elements of each
+ * output row (TL;DR; "vLLM integration": uint4, group-32, BF16 scales), and
+ * tokens routed through sorted_ids / expert_ids / num_tokens_padded built by a
+ * moe_align step ("Two kernel families": the indexed family consumes that
+ * routing; "vLLM integration": over-allocated buffers, no host read-back of
+ * the routed count, CUDA-graph capturable).  A layer is gate_up, SiLU-and-mul,
+ * down and the top-k-weighted sum ("Measurements": per-layer time is gate_up
+ * plus down; "humans& Beats FlashInfer's Best MoE Kernel by 25% on Blackwell
+ * GPUs", "Dedicated warps keep the pipeline busy": FC1, FC2, top-K merge).
+ *
+ * Conventions shared by every call below
+ *  - Every pointer named "device" is device memory owned by the caller; the
+ *    library never allocates, frees or keeps a pointer after a call returns.
+ *    Host pointers are read during the call only.
+ *  - BF16 data is passed as uint16_t bit patterns.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream).  No call synchronises the host or reads device memory back, so
+ *    every call can be captured into a CUDA graph.
+ *  - Every call returns a w4a16_status_t.  Argument errors are detected on the
+ *    host before anything is enqueued; W4A16_CUDA_ERROR means a launch failed
+ *    (the CUDA error is cleared and its text is kept for
+ *    w4a16_last_error_detail()).
+ *  - Problems found while kernels run (bad expert ids with validation on,
+ *    a bounded wait that gave up, a packed-weight header mismatch) set bits in
+ *    an optional caller-provided device int32 (`dev_err`, may be NULL); the
+ *    host reads it when it chooses.  Kernels never trap.
+ *  - Requires a GPU of compute capability 10.3 (sm_103a).
+ */
+#ifndef W4A16_MOE_H_
+#define W4A16_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* w4a16_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  W4A16_OK = 0,
+  W4A16_INVALID_ARG = 1,         /* null pointer, negative or inconsistent size */
+  W4A16_UNSUPPORTED = 2,         /* group != 32, K % 64, N % 128, block_m not in {16,32,64,128}, not sm_103 */
+  W4A16_BAD_PACKED_WEIGHT = 3,   /* packed-weight descriptor magic/version/shape/mode mismatch */
+  W4A16_WORKSPACE_TOO_SMALL = 4, /* workspace smaller than the matching *_workspace_size() */
+  W4A16_CUDA_ERROR = 5           /* a CUDA launch or attribute call failed */
+} w4a16_status_t;
+
+/* Device error bits written (OR-ed) into `dev_err` by the kernels. */
+#define W4A16_DEVERR_BAD_EXPERT_ID 0x1 /* an id outside [-1, E) was seen (treated as dropped) */
+#define W4A16_DEVERR_CAPACITY 0x2      /* padded rows exceeded capacity (extra rows dropped) */
+#define W4A16_DEVERR_TIMEOUT 0x4       /* a bounded pipeline wait gave up; output incomplete */
+#define W4A16_DEVERR_BAD_HEADER 0x8    /* the packed blob's device header does not match */
+
+/* Static text for a status code. */
+const char* w4a16_status_string(w4a16_status_t status);
+/* Text of the last failure seen by this host thread (empty if none). */
+const char* w4a16_last_error_detail(void);
+
+/* ------------------------------------------------------------------------------------------
+ * Routing alignment ("Two kernel families"; "vLLM integration").
+ *
+ * topk_ids   device int32 [T, top_k], row-major; a local expert id in [0, E) or -1 for a
+ *            dropped slot (an expert on another rank).  With validate != 0, any other value
+ *            sets W4A16_DEVERR_BAD_EXPERT_ID in *dev_err; it is always treated as dropped.
+ * Outputs (device, int32): sorted_ids [capacity], expert_ids [capacity / block_m],
+ *            num_tokens_padded [1].
+ * Result: the flat slot index i = t*top_k + s, stably sorted by expert (ascending i within an
+ * expert), each expert's run padded up to a multiple of block_m with the sentinel T*top_k;
+ * positions in [num_tokens_padded, capacity) also hold the sentinel.  expert_ids[b] is the
+ * expert of rows [b*block_m, (b+1)*block_m) for b < num_tokens_padded / block_m and -1 after.
+ * Experts with no routed slot get no block.  capacity must be a multiple of block_m and at
+ * least w4a16_align_capacity(); 1 <= E <= 1024; T*top_k < 2^31.
+ * ---------------------------------------------------------------------------------------- */
+int64_t w4a16_align_capacity(int T, int top_k, int E, int block_m);
+w4a16_status_t w4a16_moe_align(const int32_t* topk_ids, int T, int top_k, int E, int block_m,
+                               int32_t* sorted_ids, int32_t* expert_ids,
+                               int32_t* num_tokens_padded, int64_t capacity, int validate,
+                               int32_t* dev_err, w4a16_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Offline weight repack ("Grouped SM90 kernels": weights are packed once, the layout mode is
+ * recorded in the prepared weight and checked at dispatch so a mismatch fails loudly).
+ *
+ * qweight  device int32 [E, N, K/8]: uint4 codes, element k in word k/8 at bits 4*(k%8)..+3
+ *          (low nibble first); dequantised value (q - 8) * s.
+ * scales   device uint16 (BF16) [E, N, K/32]: scale of elements [32g, 32g+32) of a row.
+ * flags    W4A16_PACK_GATE_UP_PAIRED: N = 2*I holds gate rows [0, I) then up rows [I, 2I)
+ *          (I % 64 == 0); every 128-row tile then carries 64 gate and the matching 64 up rows,
+ *          which lets the GEMM fuse SiLU-and-mul.  0: plain row order.
+ * packed   device buffer of w4a16_packed_bytes() bytes, 256-byte aligned; receives a device
+ *          header and the tile stream.  `desc` (host) is filled on success and is what the
+ *          GEMM calls take.  Requires group == 32, K % 64 == 0, N % 128 == 0.
+ * Layout of the tile stream: for expert e, 128-row tile j, 64-wide K block kb, one 4608-byte
+ * chunk (codes of 128 rows x 64 K, nibble-interleaved for pairwise BF16 conversion, then the
+ * 128 x 2 scales); chunks of one (e, j) are contiguous along K.
+ * ---------------------------------------------------------------------------------------- */
+#define W4A16_PACK_GATE_UP_PAIRED 0x1u
+#define W4A16_PACK_MAGIC 0x3631413457454f4dull /* "MOEW4A16" in little-endian bytes */
+#define W4A16_PACK_VERSION 1u
+
+typedef struct {
+  uint64_t magic;   /* W4A16_PACK_MAGIC once filled */
+  uint32_t version; /* W4A16_PACK_VERSION */
+  uint32_t flags;   /* W4A16_PACK_* */
+  int32_t E, N, K, group;
+  uint64_t bytes;   /* size of the device blob */
+  const void* data; /* device pointer to the blob (header + tiles) */
+} w4a16_packed_weights_t;
+
+size_t w4a16_packed_bytes(int E, int N, int K, int group, uint32_t flags);
+w4a16_status_t w4a16_pack_weights(const int32_t* qweight, const uint16_t* scales, int E, int N,
+                                  int K, int group, uint32_t flags, void* packed,
+                                  size_t packed_bytes, w4a16_packed_weights_t* desc,
+                                  w4a16_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Indexed grouped GEMM ("Two kernel families"; "H200 and Blackwell indexed decode").
+ *
+ * For every sorted position p < *num_tokens_padded with slot i = sorted_ids[p] < total_slots
+ * and expert e = expert_ids[p / block_m]:
+ *     C[row_c(p), :] = A[row_a(p), :] . dequant(W[e])^T      (FP32 accumulation, BF16 out)
+ * row_a(p) = i / a_row_div (top_k for gate_up, 1 for down), or p with W4A16_A_ROWS_SORTED;
+ * row_c(p) = i, or p with W4A16_C_ROWS_SORTED (then padding rows p are written too, as
+ * zeros).  Rows of C not named are left untouched.
+ * A  device BF16 [rows, K] with row stride lda elements (lda % 8 == 0, 16-byte aligned rows).
+ * C  device BF16 with row stride ldc elements; N columns (epilogue NONE) or N/2 columns
+ *    (epilogue SILU_MUL: C[., j] = bf16(silu(g) * u), g and u the BF16-rounded gate and up
+ *    outputs; needs a W4A16_PACK_GATE_UP_PAIRED weight).
+ * workspace  device scratch of w4a16_gemm_workspace_size() bytes, 256-byte aligned; its
+ *    counter words must be zero before the first use (w4a16_workspace_clear, or cudaMemset)
+ *    and every call leaves them zero.  Concurrent calls must not share a workspace.
+ * expected_rows_per_expert  host hint for the schedule (0: total_slots / E); it never
+ *    changes results, which are independent of the schedule up to FP32 summation order
+ *    (and bitwise identical between runs of the same schedule).
+ * ---------------------------------------------------------------------------------------- */
+#define W4A16_EPILOGUE_NONE 0
+#define W4A16_EPILOGUE_SILU_MUL 1
+#define W4A16_A_ROWS_SORTED 0x1u
+#define W4A16_C_ROWS_SORTED 0x2u
+
+typedef struct {
+  const int32_t* sorted_ids;        /* device [capacity] */
+  const int32_t* expert_ids;        /* device [capacity / block_m] */
+  const int32_t* num_tokens_padded; /* device [1] */
+  int64_t capacity;
+  int32_t block_m;                  /* 16, 32, 64 or 128 */
+  int32_t total_slots;              /* T * top_k, the sentinel value */
+} w4a16_routing_t;
+
+/* Schedule override, for measurements only (NULL or zeros: the planner decides). */
+typedef struct {
+  int32_t split_k;  /* K slices per tile (1..16) */
+  int32_t num_ctas; /* persistent CTAs */
+} w4a16_schedule_t;
+
+size_t w4a16_gemm_workspace_size(int total_slots, int E, int N, int K, int block_m);
+w4a16_status_t w4a16_workspace_clear(void* workspace, size_t workspace_bytes,
+                                     w4a16_stream_t stream);
+w4a16_status_t w4a16_moe_gemm(const uint16_t* A, int64_t lda, int a_row_div,
+                              const w4a16_packed_weights_t* W, const w4a16_routing_t* routing,
+                              int epilogue, uint32_t row_flags, uint16_t* C, int64_t ldc,
+                              void* workspace, size_t workspace_bytes,
+                              int expected_rows_per_expert, const w4a16_schedule_t* schedule,
+                              int32_t* dev_err, w4a16_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Top-k weighted sum (the "top-K expert output merge" of the humans& page).
+ * Y device BF16 [T*top_k, H]; out[t, :] = bf16(sum over s ascending with topk_ids[t,s] >= 0
+ * of topk_weights[t,s] * Y[t*top_k + s, :]), FP32 accumulation; rows of dropped slots are
+ * not read.  H % 8 == 0.
+ * ---------------------------------------------------------------------------------------- */
+w4a16_status_t w4a16_topk_sum(const uint16_t* Y, const int32_t* topk_ids,
+                              const float* topk_weights, int T, int top_k, int H,
+                              uint16_t* out, w4a16_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Whole layer: align -> gate_up (SiLU-and-mul fused) -> down -> top-k sum, four kernels
+ * chained with programmatic dependent launch ("humans& ...", "Blackwell hides the conversion
+ * work": FC2 starts its weight work before FC1 completes).
+ * x  device BF16 [T, H]; w13 packed [E, 2I, H] with W4A16_PACK_GATE_UP_PAIRED; w2 packed
+ * [E, H, I]; topk_ids / topk_weights device [T, top_k]; out device BF16 [T, H] (a token
+ * with no local slot gets a zero row).  E_global: experts the router chose from (0 = E),
+ * used only for the schedule.  block_m: 0 = planner.  workspace of
+ * w4a16_layer_workspace_size(..) bytes with the same block_m argument; no zeroing needed.
+ * ---------------------------------------------------------------------------------------- */
+int w4a16_plan_block_m(int T, int top_k, int E, int E_global);
+size_t w4a16_layer_workspace_size(int T, int top_k, int E, int E_global, int H, int I,
+                                  int block_m);
+w4a16_status_t w4a16_moe_layer(const uint16_t* x, const w4a16_packed_weights_t* w13,
+                               const w4a16_packed_weights_t* w2, const int32_t* topk_ids,
+                               const float* topk_weights, int T, int top_k, int E_global,
+                               int block_m, uint16_t* out, void* workspace,
+                               size_t workspace_bytes, int32_t* dev_err, w4a16_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Host planner (no device work; usable without a GPU): the schedule w4a16_moe_gemm would
+ * pick for these sizes on a GPU with num_sms SMs.
+ * ---------------------------------------------------------------------------------------- */
+typedef struct {
+  int32_t block_m;
+  int32_t split_k;
+  int32_t num_ctas;
+  int32_t stages;      /* weight/activation ring depth in shared memory */
+  int32_t est_units;   /* estimated (block, tile, split) work units */
+} w4a16_plan_t;
+
+w4a16_status_t w4a16_plan_gemm(int total_slots, int E, int N, int K, int block_m,
+                               int expected_rows_per_expert, int num_sms, w4a16_plan_t* plan);
+
+/* ------------------------------------------------------------------------------------------
+ * Test hook: dequantise expert `expert` of a packed weight with the GEMM's own device
+ * conversion routine, into canonical order out device BF16 [N, K].
+ * ---------------------------------------------------------------------------------------- */
+w4a16_status_t w4a16_debug_dequant(const w4a16_packed_weights_t* W, int expert, uint16_t* out,
+                                   w4a16_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_MOE_H_ */

@@ -1,0 +1,337 @@
+"""Python binding of the GB300 W4A16 MoE expert library (ctypes over the C ABI).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels (``csrc/``, built for sm_103a into ``_build/libw4a16_moe.so``).  There is
+no CPU fallback: if the library is missing or fails to load, every call raises.
+PyTorch provides device memory and streams; calls are enqueued on the current
+torch CUDA stream.
+
+The C ABI is declared, with argument meaning, layouts and error behaviour, in
+``include/w4a16_moe.h``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "load", "library_path", "align_capacity", "moe_align", "PackedWeights", "pack_weights",
+    "Routing", "moe_gemm", "topk_sum", "moe_layer", "layer_workspace_size", "plan_block_m",
+    "plan_gemm", "debug_dequant", "gemm_workspace_size", "EPILOGUE_NONE", "EPILOGUE_SILU_MUL",
+    "A_ROWS_SORTED", "C_ROWS_SORTED", "PACK_GATE_UP_PAIRED", "LibraryError",
+]
+
+EPILOGUE_NONE = 0
+EPILOGUE_SILU_MUL = 1
+A_ROWS_SORTED = 0x1
+C_ROWS_SORTED = 0x2
+PACK_GATE_UP_PAIRED = 0x1
+PACK_MAGIC = 0x3631413457454F4D
+PACK_VERSION = 1
+
+DEVERR_BAD_EXPERT_ID = 0x1
+DEVERR_CAPACITY = 0x2
+DEVERR_TIMEOUT = 0x4
+DEVERR_BAD_HEADER = 0x8
+
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "bad packed weight",
+           4: "workspace too small", 5: "CUDA error"}
+
+
+class LibraryError(RuntimeError):
+    def __init__(self, fn: str, status: int, detail: str):
+        super().__init__(f"{fn}: {_STATUS.get(status, status)} ({detail})")
+        self.status = status
+
+
+class PackedDesc(ctypes.Structure):
+    _fields_ = [("magic", ctypes.c_uint64), ("version", ctypes.c_uint32), ("flags", ctypes.c_uint32),
+                ("E", ctypes.c_int32), ("N", ctypes.c_int32), ("K", ctypes.c_int32),
+                ("group", ctypes.c_int32), ("bytes", ctypes.c_uint64), ("data", ctypes.c_void_p)]
+
+
+class RoutingDesc(ctypes.Structure):
+    _fields_ = [("sorted_ids", ctypes.c_void_p), ("expert_ids", ctypes.c_void_p),
+                ("num_tokens_padded", ctypes.c_void_p), ("capacity", ctypes.c_int64),
+                ("block_m", ctypes.c_int32), ("total_slots", ctypes.c_int32)]
+
+
+class ScheduleDesc(ctypes.Structure):
+    _fields_ = [("split_k", ctypes.c_int32), ("num_ctas", ctypes.c_int32)]
+
+
+class PlanDesc(ctypes.Structure):
+    _fields_ = [("block_m", ctypes.c_int32), ("split_k", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("est_units", ctypes.c_int32)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+_VP, _I32, _I64, _U32, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint32, ctypes.c_size_t
+_P = ctypes.POINTER
+_SIGNATURES = {
+    "w4a16_status_string": (ctypes.c_char_p, [_I32]),
+    "w4a16_last_error_detail": (ctypes.c_char_p, []),
+    "w4a16_align_capacity": (_I64, [_I32, _I32, _I32, _I32]),
+    "w4a16_moe_align": (_I32, [_VP, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _I64, _I32, _VP, _VP]),
+    "w4a16_packed_bytes": (_SZ, [_I32, _I32, _I32, _I32, _U32]),
+    "w4a16_pack_weights": (_I32, [_VP, _VP, _I32, _I32, _I32, _I32, _U32, _VP, _SZ, _P(PackedDesc), _VP]),
+    "w4a16_gemm_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
+    "w4a16_workspace_clear": (_I32, [_VP, _SZ, _VP]),
+    "w4a16_moe_gemm": (_I32, [_VP, _I64, _I32, _P(PackedDesc), _P(RoutingDesc), _I32, _U32, _VP, _I64,
+                              _VP, _SZ, _I32, _P(ScheduleDesc), _VP, _VP]),
+    "w4a16_topk_sum": (_I32, [_VP, _VP, _VP, _I32, _I32, _I32, _VP, _VP]),
+    "w4a16_plan_block_m": (_I32, [_I32, _I32, _I32, _I32]),
+    "w4a16_layer_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32, _I32]),
+    "w4a16_moe_layer": (_I32, [_VP, _P(PackedDesc), _P(PackedDesc), _VP, _VP, _I32, _I32, _I32, _I32,
+                               _VP, _VP, _SZ, _VP, _VP]),
+    "w4a16_plan_gemm": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _P(PlanDesc)]),
+    "w4a16_debug_dequant": (_I32, [_P(PackedDesc), _I32, _VP, _VP]),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load the CUDA library (building it first if asked and needed)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path):
+                if not build_if_missing:
+                    raise RuntimeError(f"CUDA library not built: {path} (run __graft_entry__.build())")
+                _build.build()
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        detail = load().w4a16_last_error_detail().decode(errors="replace")
+        raise LibraryError(fn, status, detail)
+
+
+def _stream(stream=None) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _cuda(t: torch.Tensor, dtype: torch.dtype, name: str) -> torch.Tensor:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+# ---- routing -------------------------------------------------------------------------------
+
+def align_capacity(T: int, top_k: int, E: int, block_m: int) -> int:
+    return int(load().w4a16_align_capacity(T, top_k, E, block_m))
+
+
+@dataclass
+class Routing:
+    sorted_ids: torch.Tensor
+    expert_ids: torch.Tensor
+    num_tokens_padded: torch.Tensor
+    block_m: int
+    total_slots: int
+
+    @property
+    def capacity(self) -> int:
+        return self.sorted_ids.numel()
+
+    def desc(self) -> RoutingDesc:
+        return RoutingDesc(self.sorted_ids.data_ptr(), self.expert_ids.data_ptr(),
+                           self.num_tokens_padded.data_ptr(), self.capacity, self.block_m,
+                           self.total_slots)
+
+
+def moe_align(topk_ids: torch.Tensor, E: int, block_m: int, capacity: Optional[int] = None,
+              validate: bool = False, dev_err: Optional[torch.Tensor] = None) -> Routing:
+    _cuda(topk_ids, torch.int32, "topk_ids")
+    T, k = topk_ids.shape
+    cap = align_capacity(T, k, E, block_m) if capacity is None else capacity
+    dev = topk_ids.device
+    sorted_ids = torch.empty(cap, dtype=torch.int32, device=dev)
+    expert_ids = torch.empty(cap // block_m, dtype=torch.int32, device=dev)
+    ntp = torch.empty(1, dtype=torch.int32, device=dev)
+    _check("w4a16_moe_align", load().w4a16_moe_align(
+        _ptr(topk_ids), T, k, E, block_m, _ptr(sorted_ids), _ptr(expert_ids), _ptr(ntp), cap,
+        1 if validate else 0, _ptr(dev_err), _stream()))
+    return Routing(sorted_ids, expert_ids, ntp, block_m, T * k)
+
+
+# ---- weights -------------------------------------------------------------------------------
+
+class PackedWeights:
+    """A packed weight blob in device memory plus its host descriptor."""
+
+    def __init__(self, blob: torch.Tensor, desc: PackedDesc):
+        self.blob = blob
+        self.desc = desc
+
+    @property
+    def E(self):
+        return self.desc.E
+
+    @property
+    def N(self):
+        return self.desc.N
+
+    @property
+    def K(self):
+        return self.desc.K
+
+    @property
+    def paired(self) -> bool:
+        return bool(self.desc.flags & PACK_GATE_UP_PAIRED)
+
+    @property
+    def nbytes(self) -> int:
+        return int(self.desc.bytes)
+
+
+def packed_bytes(E: int, N: int, K: int, paired: bool = False) -> int:
+    return int(load().w4a16_packed_bytes(E, N, K, 32, PACK_GATE_UP_PAIRED if paired else 0))
+
+
+def pack_weights(qweight: torch.Tensor, scales: torch.Tensor, paired: bool = False) -> PackedWeights:
+    """Repack canonical int32 [E, N, K/8] codes and BF16 [E, N, K/32] scales for the GEMM."""
+    _cuda(qweight, torch.int32, "qweight")
+    _cuda(scales, torch.bfloat16, "scales")
+    E, N, K8 = qweight.shape
+    K = K8 * 8
+    if tuple(scales.shape) != (E, N, K // 32):
+        raise ValueError(f"scales must be [E, N, K/32] = {(E, N, K // 32)}, got {tuple(scales.shape)}")
+    flags = PACK_GATE_UP_PAIRED if paired else 0
+    nbytes = int(load().w4a16_packed_bytes(E, N, K, 32, flags))
+    if nbytes == 0:
+        raise LibraryError("w4a16_packed_bytes", 2, f"unsupported shape E={E} N={N} K={K}")
+    blob = torch.empty(nbytes, dtype=torch.uint8, device=qweight.device)
+    desc = PackedDesc()
+    _check("w4a16_pack_weights", load().w4a16_pack_weights(
+        _ptr(qweight), _ptr(scales), E, N, K, 32, flags, _ptr(blob), nbytes, ctypes.byref(desc),
+        _stream()))
+    return PackedWeights(blob, desc)
+
+
+def debug_dequant(W: PackedWeights, expert: int) -> torch.Tensor:
+    out = torch.empty((W.N, W.K), dtype=torch.bfloat16, device=W.blob.device)
+    _check("w4a16_debug_dequant", load().w4a16_debug_dequant(
+        ctypes.byref(W.desc), expert, _ptr(out), _stream()))
+    return out
+
+
+# ---- GEMM ----------------------------------------------------------------------------------
+
+def gemm_workspace_size(total_slots: int, E: int, N: int, K: int, block_m: int) -> int:
+    return int(load().w4a16_gemm_workspace_size(total_slots, E, N, K, block_m))
+
+
+def gemm_workspace(total_slots: int, E: int, N: int, K: int, block_m: int, device) -> torch.Tensor:
+    """A zeroed workspace (its counters must start at zero; calls leave them zero)."""
+    return torch.zeros(gemm_workspace_size(total_slots, E, N, K, block_m), dtype=torch.uint8,
+                       device=device)
+
+
+def moe_gemm(A: torch.Tensor, a_row_div: int, W: PackedWeights, routing: Routing,
+             epilogue: int = EPILOGUE_NONE, row_flags: int = 0, out: Optional[torch.Tensor] = None,
+             out_rows: Optional[int] = None, workspace: Optional[torch.Tensor] = None,
+             expected_rows_per_expert: int = 0, split_k: int = 0, num_ctas: int = 0,
+             dev_err: Optional[torch.Tensor] = None) -> torch.Tensor:
+    _cuda(A, torch.bfloat16, "A")
+    width = W.N // 2 if epilogue == EPILOGUE_SILU_MUL else W.N
+    if out is None:
+        rows = out_rows if out_rows is not None else (
+            routing.capacity if row_flags & C_ROWS_SORTED else routing.total_slots)
+        out = torch.zeros((rows, width), dtype=torch.bfloat16, device=A.device)
+    _cuda(out, torch.bfloat16, "out")
+    if workspace is None:
+        workspace = gemm_workspace(routing.total_slots, W.E, W.N, W.K, routing.block_m, A.device)
+    sched = ScheduleDesc(split_k, num_ctas)
+    rd = routing.desc()
+    _check("w4a16_moe_gemm", load().w4a16_moe_gemm(
+        _ptr(A), A.stride(0), a_row_div, ctypes.byref(W.desc), ctypes.byref(rd), epilogue, row_flags,
+        _ptr(out), out.stride(0), _ptr(workspace), workspace.numel(), expected_rows_per_expert,
+        ctypes.byref(sched), _ptr(dev_err), _stream()))
+    return out
+
+
+def topk_sum(Y: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+             out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    _cuda(Y, torch.bfloat16, "Y")
+    _cuda(topk_ids, torch.int32, "topk_ids")
+    _cuda(topk_weights, torch.float32, "topk_weights")
+    T, k = topk_ids.shape
+    H = Y.shape[1]
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=Y.device)
+    _check("w4a16_topk_sum", load().w4a16_topk_sum(
+        _ptr(Y), _ptr(topk_ids), _ptr(topk_weights), T, k, H, _ptr(out), _stream()))
+    return out
+
+
+# ---- layer ---------------------------------------------------------------------------------
+
+def plan_block_m(T: int, top_k: int, E: int, E_global: int = 0) -> int:
+    return int(load().w4a16_plan_block_m(T, top_k, E, E_global))
+
+
+def layer_workspace_size(T: int, top_k: int, E: int, H: int, I: int, E_global: int = 0,
+                         block_m: int = 0) -> int:
+    return int(load().w4a16_layer_workspace_size(T, top_k, E, E_global, H, I, block_m))
+
+
+def moe_layer(x: torch.Tensor, w13: PackedWeights, w2: PackedWeights, topk_ids: torch.Tensor,
+              topk_weights: torch.Tensor, E_global: int = 0, block_m: int = 0,
+              out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+              dev_err: Optional[torch.Tensor] = None) -> torch.Tensor:
+    _cuda(x, torch.bfloat16, "x")
+    _cuda(topk_ids, torch.int32, "topk_ids")
+    _cuda(topk_weights, torch.float32, "topk_weights")
+    T, H = x.shape
+    k = topk_ids.shape[1]
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    need = layer_workspace_size(T, k, w13.E, H, w13.N // 2, E_global, block_m)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    _check("w4a16_moe_layer", load().w4a16_moe_layer(
+        _ptr(x), ctypes.byref(w13.desc), ctypes.byref(w2.desc), _ptr(topk_ids), _ptr(topk_weights),
+        T, k, E_global, block_m, _ptr(out), _ptr(workspace), workspace.numel(), _ptr(dev_err),
+        _stream()))
+    return out
+
+
+# ---- host planner --------------------------------------------------------------------------
+
+def plan_gemm(total_slots: int, E: int, N: int, K: int, block_m: int, num_sms: int,
+              expected_rows_per_expert: int = 0) -> dict:
+    p = PlanDesc()
+    _check("w4a16_plan_gemm", load().w4a16_plan_gemm(
+        total_slots, E, N, K, block_m, expected_rows_per_expert, num_sms, ctypes.byref(p)))
+    return {f: getattr(p, f) for f, _ in PlanDesc._fields_}

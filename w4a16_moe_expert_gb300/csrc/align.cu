@@ -1,0 +1,169 @@
+// moe_align on the GPU: stable counting sort of the flat slot index by expert.
+//
+// "vLLM x Novita AI: Chord, Faster INT4 MoE for Kimi K2.x", "Two kernel families" and
+// "vLLM integration": the indexed kernels consume sorted_ids / expert_ids /
+// num_tokens_padded from an over-allocated align step, read on the device only, so the
+// whole path stays CUDA-graph capturable.
+//
+// One CTA of 1024 threads.  Each of the 32 warps owns a contiguous range of slots, which
+// keeps the sort stable without a global sort: a warp counts its range per expert, the
+// per-expert counts are scanned over warps and experts, and each warp then places its slots
+// in order (a warp-wide match gives each slot its rank among equal ids).
+#include "common.cuh"
+
+namespace w4a16 {
+
+constexpr int kAlignThreads = 1024;
+constexpr int kAlignWarps = kAlignThreads / 32;
+
+__global__ void __launch_bounds__(kAlignThreads, 1)
+    moe_align_kernel(const int32_t* __restrict__ topk_ids, int n_slots, int E, int block_m,
+                     int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids,
+                     int32_t* __restrict__ ntp_out, int64_t capacity, int validate,
+                     int32_t* dev_err, int32_t* zero_words, int n_zero_words) {
+  extern __shared__ int32_t sm[];
+  int32_t* cnt = sm;                      // [32][E]: per-warp counts, later per-warp cursors
+  int32_t* start = sm + kAlignWarps * E;  // [E + 1]: padded exclusive prefix
+  __shared__ int32_t warp_sums[kAlignWarps];
+  __shared__ int bad_id;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int32_t sentinel = n_slots;
+  pdl_launch_dependents();  // the next kernel may start its prologue; it waits for our results
+  pdl_wait();               // topk_ids may come from the previous kernel in the stream
+
+  for (int i = tid; i < kAlignWarps * E; i += kAlignThreads) cnt[i] = 0;
+  if (tid == 0) bad_id = 0;
+  for (int i = tid; i < n_zero_words; i += kAlignThreads) zero_words[i] = 0;
+  // all rows start as sentinels; real slots overwrite them after the barriers below
+  for (int64_t p = tid; p < capacity; p += kAlignThreads) sorted_ids[p] = sentinel;
+  __syncthreads();
+
+  // ---- count per (warp, expert) ----
+  const int per_warp = ((n_slots + kAlignWarps - 1) / kAlignWarps + 31) & ~31;
+  const int lo = warp * per_warp;
+  const int hi = min(n_slots, lo + per_warp);
+  for (int base = lo; base < hi; base += 32) {
+    const int i = base + lane;
+    int e = (i < hi) ? topk_ids[i] : -1;
+    if (e < -1 || e >= E) {
+      if (validate) bad_id = 1;
+      e = -1;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) cnt[warp * E + e] += __popc(peers);
+  }
+  __syncthreads();
+
+  // ---- per expert: totals, warp offsets inside the expert, padded size ----
+  for (int e = tid; e < E; e += kAlignThreads) {
+    int run = 0;
+    for (int w = 0; w < kAlignWarps; ++w) {
+      const int c = cnt[w * E + e];
+      cnt[w * E + e] = run;
+      run += c;
+    }
+    start[e] = (run + block_m - 1) / block_m * block_m;  // padded size for now
+  }
+  __syncthreads();
+
+  // ---- exclusive scan of padded sizes over experts (E <= 1024: one element per thread) ----
+  {
+    const int v = (tid < E) ? start[tid] : 0;
+    int x = v;
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int s = warp_sums[lane];
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, s, off);
+        if (lane >= off) s += y;
+      }
+      warp_sums[lane] = s;  // inclusive over warps
+    }
+    __syncthreads();
+    const int excl = x - v + (warp > 0 ? warp_sums[warp - 1] : 0);
+    __syncthreads();
+    if (tid < E) start[tid] = excl;
+    if (tid == 0) start[E] = warp_sums[kAlignWarps - 1];
+  }
+  __syncthreads();
+  const int ntp = start[E];
+
+  // ---- per-warp cursors become absolute positions ----
+  for (int i = tid; i < kAlignWarps * E; i += kAlignThreads) cnt[i] += start[i % E];
+  // ---- expert of every block ----
+  const int64_t nblocks = capacity / block_m;
+  for (int64_t b = tid; b < nblocks; b += kAlignThreads) {
+    const int64_t row = b * block_m;
+    int owner = -1;
+    if (row < ntp) {  // last expert whose start is <= row (experts with no rows have size 0)
+      int l = 0, h = E - 1;
+      while (l < h) {
+        const int mid = (l + h + 1) >> 1;
+        if (start[mid] <= row) l = mid; else h = mid - 1;
+      }
+      owner = l;
+    }
+    expert_ids[b] = owner;
+  }
+  __syncthreads();
+
+  // ---- stable placement ----
+  bool overflow = false;
+  for (int base = lo; base < hi; base += 32) {
+    const int i = base + lane;
+    int e = (i < hi) ? topk_ids[i] : -1;
+    if (e < -1 || e >= E) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0) {
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      const int pos = cnt[warp * E + e] + rank;
+      if (pos < capacity) sorted_ids[pos] = i; else overflow = true;
+    }
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) cnt[warp * E + e] += __popc(peers);
+    __syncwarp();
+  }
+  if (overflow) set_dev_err(dev_err, W4A16_DEVERR_CAPACITY);
+  if (tid == 0) {
+    *ntp_out = (ntp <= capacity) ? ntp : static_cast<int32_t>(capacity / block_m * block_m);
+    if (ntp > capacity) set_dev_err(dev_err, W4A16_DEVERR_CAPACITY);
+  }
+  __syncthreads();
+  if (tid == 0 && bad_id) set_dev_err(dev_err, W4A16_DEVERR_BAD_EXPERT_ID);
+}
+
+size_t align_smem_bytes(int E) {
+  return static_cast<size_t>(kAlignWarps * E + E + 1) * sizeof(int32_t);
+}
+
+cudaError_t launch_moe_align(const int32_t* topk_ids, int n_slots, int E, int block_m,
+                             int32_t* sorted_ids, int32_t* expert_ids, int32_t* ntp,
+                             int64_t capacity, int validate, int32_t* dev_err,
+                             int32_t* zero_words, int n_zero_words, cudaStream_t stream) {
+  const size_t smem = align_smem_bytes(E);
+  cudaError_t err = cudaFuncSetAttribute(moe_align_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(kAlignThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, moe_align_kernel, topk_ids, n_slots, E, block_m, sorted_ids,
+                            expert_ids, ntp, capacity, validate, dev_err, zero_words,
+                            n_zero_words);
+}
+
+}  // namespace w4a16

@@ -1,0 +1,503 @@
+// C ABI of the library (declared in include/w4a16_moe.h): argument checks, workspace
+// layout, the host planner, the top-k combine kernel and the layer chain.
+#include <algorithm>
+#include <cstdarg>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "gemm.cuh"
+
+namespace w4a16 {
+
+// kernels and launchers defined in the other translation units
+cudaError_t launch_moe_align(const int32_t* topk_ids, int n_slots, int E, int block_m,
+                             int32_t* sorted_ids, int32_t* expert_ids, int32_t* ntp,
+                             int64_t capacity, int validate, int32_t* dev_err,
+                             int32_t* zero_words, int n_zero_words, cudaStream_t stream);
+size_t align_smem_bytes(int E);
+cudaError_t launch_pack(const int32_t* qweight, const uint16_t* scales, int E, int N, int K,
+                        uint32_t flags, void* packed, cudaStream_t stream);
+cudaError_t launch_debug_dequant(const void* packed, int e, int N, int K, uint32_t flags,
+                                 uint16_t* out, cudaStream_t stream);
+
+
+// ---- error bookkeeping ------------------------------------------------------------------------
+static thread_local char g_detail[512] = "";
+
+static w4a16_status_t fail(w4a16_status_t st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_detail, sizeof g_detail, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+static w4a16_status_t cuda_fail(cudaError_t err, const char* what) {
+  cudaGetLastError();  // clear the sticky-free launch error
+  return fail(W4A16_CUDA_ERROR, "%s: %s", what, cudaGetErrorString(err));
+}
+
+// ---- device facts (cached per device) -----------------------------------------------------------
+struct DeviceFacts {
+  int checked = 0;
+  int ok = 0;
+  int num_sms = 0;
+};
+static DeviceFacts g_dev[64];
+static std::mutex g_dev_mu;
+
+static w4a16_status_t device_facts(DeviceFacts* out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(W4A16_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceFacts& f = g_dev[dev];
+  if (!f.checked) {
+    int major = 0, minor = 0, sms = 0;
+    if ((err = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(err, "cudaDeviceGetAttribute");
+    f.ok = (major == 10 && minor == 3);
+    f.num_sms = sms;
+    f.checked = 1;
+  }
+  if (!f.ok) return fail(W4A16_UNSUPPORTED, "this library is built for sm_103a (GB300) only");
+  *out = f;
+  return W4A16_OK;
+}
+
+static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+static bool valid_block_m(int bm) { return bm == 16 || bm == 32 || bm == 64 || bm == 128; }
+
+// K-split scratch: a fixed 16 MB of FP32 partials, i.e. 32768 / block_m (tile, split) units.
+constexpr size_t kPartialBytes = size_t(16) << 20;
+static int64_t split_unit_budget(int block_m) { return 32768 / block_m; }
+
+static w4a16_status_t check_packed(const w4a16_packed_weights_t* W) {
+  if (!W) return fail(W4A16_INVALID_ARG, "packed weight descriptor is NULL");
+  if (W->magic != W4A16_PACK_MAGIC || W->version != W4A16_PACK_VERSION)
+    return fail(W4A16_BAD_PACKED_WEIGHT, "packed weight descriptor has a bad magic or version");
+  if (W->group != 32 || W->K % kBlockK || W->N % kTileRows || W->E < 0 || !W->data)
+    return fail(W4A16_BAD_PACKED_WEIGHT, "packed weight descriptor has bad sizes");
+  if (reinterpret_cast<uintptr_t>(W->data) % 256)
+    return fail(W4A16_BAD_PACKED_WEIGHT, "packed weight blob must be 256-byte aligned");
+  return W4A16_OK;
+}
+
+// ---- top-k weighted sum ---------------------------------------------------------------------------
+// One thread per 8 output columns of one token; FP32 accumulation over slots in order.
+__global__ void __launch_bounds__(256)
+    topk_sum_kernel(const uint16_t* __restrict__ Y, const int32_t* __restrict__ topk_ids,
+                    const float* __restrict__ topk_weights, int T, int top_k, int H,
+                    uint16_t* __restrict__ out) {
+  pdl_wait();  // Y is the previous kernel's output
+  const int vec_per_row = H / 8;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<int64_t>(T) * vec_per_row) return;
+  const int64_t t = idx / vec_per_row;
+  const int c = static_cast<int>(idx % vec_per_row) * 8;
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int s = 0; s < top_k; ++s) {
+    const int64_t i = t * top_k + s;
+    if (__ldg(topk_ids + i) < 0) continue;
+    const float w = __ldg(topk_weights + i);
+    const uint4 y = __ldg(reinterpret_cast<const uint4*>(Y + i * H + c));
+    const uint32_t yw[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      acc[2 * q] += w * __uint_as_float(yw[q] << 16);
+      acc[2 * q + 1] += w * __uint_as_float(yw[q] & 0xffff0000u);
+    }
+  }
+  uint32_t o[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * q]));
+    const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * q + 1]));
+    o[q] = lo | (hi << 16);
+  }
+  *reinterpret_cast<uint4*>(out + t * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+static cudaError_t launch_topk_sum(const uint16_t* Y, const int32_t* ids, const float* w, int T,
+                                   int top_k, int H, uint16_t* out, cudaStream_t stream) {
+  const int64_t n = static_cast<int64_t>(T) * (H / 8);
+  if (n == 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((n + 255) / 256));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, topk_sum_kernel, Y, ids, w, T, top_k, H, out);
+}
+
+// ---- GEMM call shared by the ABI entry and the layer ----------------------------------------------
+struct GemmCall {
+  const uint16_t* A;
+  int64_t lda;
+  int a_row_div;
+  const w4a16_packed_weights_t* W;
+  const w4a16_routing_t* R;
+  int epilogue;
+  uint32_t row_flags;
+  uint16_t* C;
+  int64_t ldc;
+  void* ws;
+  size_t ws_bytes;
+  int rows_hint;
+  const w4a16_schedule_t* sched;
+  int32_t* dev_err;
+  int routing_ready;
+};
+
+static w4a16_status_t run_gemm(const GemmCall& c, const DeviceFacts& dev, cudaStream_t stream) {
+  w4a16_status_t st = check_packed(c.W);
+  if (st != W4A16_OK) return st;
+  const w4a16_routing_t* R = c.R;
+  if (!R || !R->sorted_ids || !R->expert_ids || !R->num_tokens_padded)
+    return fail(W4A16_INVALID_ARG, "routing tensors must not be NULL");
+  if (!valid_block_m(R->block_m))
+    return fail(W4A16_UNSUPPORTED, "block_m %d: supported values are 16, 32, 64, 128", R->block_m);
+  if (R->capacity < 0 || R->capacity % R->block_m || R->total_slots < 0)
+    return fail(W4A16_INVALID_ARG, "capacity must be a non-negative multiple of block_m");
+  if (!c.A || !c.C || c.a_row_div <= 0 || c.lda < c.W->K || c.lda % 8 ||
+      reinterpret_cast<uintptr_t>(c.A) % 16)
+    return fail(W4A16_INVALID_ARG, "A must be 16-byte aligned with lda >= K and lda %% 8 == 0");
+  const bool paired = (c.W->flags & W4A16_PACK_GATE_UP_PAIRED) != 0;
+  int out_cols = c.W->N;
+  if (c.epilogue == W4A16_EPILOGUE_SILU_MUL) {
+    if (!paired)
+      return fail(W4A16_BAD_PACKED_WEIGHT, "SiLU-and-mul needs a W4A16_PACK_GATE_UP_PAIRED weight");
+    out_cols = c.W->N / 2;
+  } else if (c.epilogue != W4A16_EPILOGUE_NONE) {
+    return fail(W4A16_INVALID_ARG, "unknown epilogue %d", c.epilogue);
+  }
+  if (c.ldc < out_cols) return fail(W4A16_INVALID_ARG, "ldc smaller than the output width");
+  if (R->capacity == 0 || c.W->E == 0) return W4A16_OK;
+
+  w4a16_plan_t plan;
+  plan_gemm(R->total_slots, c.W->E, c.W->N, c.W->K, R->block_m, c.rows_hint, dev.num_sms, &plan);
+  int split = plan.split_k, grid = plan.num_ctas;
+  const int n_kb = c.W->K / kBlockK;
+  if (c.sched && c.sched->split_k > 0) split = c.sched->split_k;
+  if (c.sched && c.sched->num_ctas > 0) grid = c.sched->num_ctas;
+  split = std::max(1, std::min(split, std::min(16, n_kb)));
+  grid = std::max(1, std::min(grid, dev.num_sms));
+
+  const int64_t budget = split_unit_budget(R->block_m);
+  const size_t cnt_bytes = round_up(static_cast<size_t>(budget) * sizeof(int32_t), 256);
+  if (split > 1 && (!c.ws || c.ws_bytes < cnt_bytes + kPartialBytes))
+    return fail(W4A16_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes", cnt_bytes + kPartialBytes);
+
+  GemmArgs a{};
+  a.A = c.A;
+  a.lda = c.lda;
+  a.a_row_div = c.a_row_div;
+  a.a_sorted = (c.row_flags & W4A16_A_ROWS_SORTED) ? 1 : 0;
+  a.wblob = static_cast<const uint8_t*>(c.W->data);
+  a.E = c.W->E;
+  a.N = c.W->N;
+  a.K = c.W->K;
+  a.n_tiles = c.W->N / kTileRows;
+  a.n_kb = n_kb;
+  a.paired = paired ? 1 : 0;
+  a.sorted_ids = R->sorted_ids;
+  a.expert_ids = R->expert_ids;
+  a.ntp = R->num_tokens_padded;
+  a.block_m = R->block_m;
+  a.total_slots = R->total_slots;
+  a.capacity = R->capacity;
+  a.epilogue = c.epilogue;
+  a.c_sorted = (c.row_flags & W4A16_C_ROWS_SORTED) ? 1 : 0;
+  a.C = c.C;
+  a.ldc = c.ldc;
+  a.cnt = static_cast<int32_t*>(c.ws);
+  a.part = c.ws ? reinterpret_cast<float*>(static_cast<uint8_t*>(c.ws) + cnt_bytes) : nullptr;
+  a.split_k = split;
+  a.max_split_units = budget;
+  a.dev_err = c.dev_err;
+  // weights streamed once per call (few rows per expert) are marked evict-first in L2
+  a.evict_first = (c.rows_hint > 0 ? c.rows_hint : R->total_slots / std::max(1, c.W->E)) <= R->block_m;
+  a.routing_ready = c.routing_ready;
+  cudaError_t err = launch_gemm(a, grid, true, stream);
+  if (err != cudaSuccess) return cuda_fail(err, "moe_gemm launch");
+  return W4A16_OK;
+}
+
+}  // namespace w4a16
+
+using namespace w4a16;
+
+extern "C" {
+
+const char* w4a16_status_string(w4a16_status_t s) {
+  switch (s) {
+    case W4A16_OK: return "ok";
+    case W4A16_INVALID_ARG: return "invalid argument";
+    case W4A16_UNSUPPORTED: return "unsupported shape, option or device";
+    case W4A16_BAD_PACKED_WEIGHT: return "bad packed weight";
+    case W4A16_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case W4A16_CUDA_ERROR: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+const char* w4a16_last_error_detail(void) { return g_detail; }
+
+int64_t w4a16_align_capacity(int T, int top_k, int E, int block_m) {
+  if (T < 0 || top_k <= 0 || E <= 0 || block_m <= 0) return -1;
+  const int64_t raw = static_cast<int64_t>(T) * top_k + static_cast<int64_t>(E) * (block_m - 1);
+  return (raw + block_m - 1) / block_m * block_m;
+}
+
+w4a16_status_t w4a16_moe_align(const int32_t* topk_ids, int T, int top_k, int E, int block_m,
+                               int32_t* sorted_ids, int32_t* expert_ids,
+                               int32_t* num_tokens_padded, int64_t capacity, int validate,
+                               int32_t* dev_err, w4a16_stream_t stream) {
+  if (T < 0 || top_k <= 0 || E <= 0 || E > 1024 || block_m <= 0)
+    return fail(W4A16_INVALID_ARG, "need T >= 0, top_k > 0, 1 <= E <= 1024, block_m > 0");
+  if (static_cast<int64_t>(T) * top_k >= (int64_t(1) << 31))
+    return fail(W4A16_INVALID_ARG, "T * top_k must be below 2^31");
+  if (capacity % block_m || capacity < w4a16_align_capacity(T, top_k, E, block_m) ||
+      capacity >= (int64_t(1) << 31))
+    return fail(W4A16_INVALID_ARG, "capacity must be a multiple of block_m, at least "
+                "w4a16_align_capacity() and below 2^31");
+  if (!sorted_ids || !expert_ids || !num_tokens_padded || (T > 0 && !topk_ids))
+    return fail(W4A16_INVALID_ARG, "NULL routing buffer");
+  DeviceFacts dev;
+  w4a16_status_t st = device_facts(&dev);
+  if (st != W4A16_OK) return st;
+  cudaError_t err = launch_moe_align(topk_ids, T * top_k, E, block_m, sorted_ids, expert_ids,
+                                     num_tokens_padded, capacity, validate, dev_err, nullptr, 0,
+                                     stream);
+  if (err != cudaSuccess) return cuda_fail(err, "moe_align launch");
+  return W4A16_OK;
+}
+
+size_t w4a16_packed_bytes(int E, int N, int K, int group, uint32_t flags) {
+  (void)flags;
+  if (E < 0 || N <= 0 || K <= 0 || group != 32 || K % kBlockK || N % kTileRows) return 0;
+  return kHeaderBytes + static_cast<size_t>(E) * (N / kTileRows) * (K / kBlockK) * kChunkBytes;
+}
+
+w4a16_status_t w4a16_pack_weights(const int32_t* qweight, const uint16_t* scales, int E, int N,
+                                  int K, int group, uint32_t flags, void* packed,
+                                  size_t packed_bytes, w4a16_packed_weights_t* desc,
+                                  w4a16_stream_t stream) {
+  if (group != 32) return fail(W4A16_UNSUPPORTED, "only group size 32 is supported");
+  if (E < 0 || N <= 0 || K <= 0 || K % kBlockK || N % kTileRows)
+    return fail(W4A16_UNSUPPORTED, "need K %% 64 == 0 and N %% 128 == 0 (got N=%d K=%d)", N, K);
+  if (flags & ~W4A16_PACK_GATE_UP_PAIRED) return fail(W4A16_INVALID_ARG, "unknown pack flags");
+  if ((flags & W4A16_PACK_GATE_UP_PAIRED) && (N % 2 || (N / 2) % 64))
+    return fail(W4A16_UNSUPPORTED, "gate/up pairing needs I = N/2 to be a multiple of 64");
+  const size_t need = w4a16_packed_bytes(E, N, K, group, flags);
+  if (!packed || !desc || (E > 0 && (!qweight || !scales)))
+    return fail(W4A16_INVALID_ARG, "NULL pointer");
+  if (packed_bytes < need) return fail(W4A16_INVALID_ARG, "packed buffer needs %zu bytes", need);
+  if (reinterpret_cast<uintptr_t>(packed) % 256 || reinterpret_cast<uintptr_t>(qweight) % 16)
+    return fail(W4A16_INVALID_ARG, "packed must be 256-byte and qweight 16-byte aligned");
+  DeviceFacts dev;
+  w4a16_status_t st = device_facts(&dev);
+  if (st != W4A16_OK) return st;
+  cudaError_t err = launch_pack(qweight, scales, E, N, K, flags, packed, stream);
+  if (err != cudaSuccess) return cuda_fail(err, "pack launch");
+  desc->magic = W4A16_PACK_MAGIC;
+  desc->version = W4A16_PACK_VERSION;
+  desc->flags = flags;
+  desc->E = E;
+  desc->N = N;
+  desc->K = K;
+  desc->group = group;
+  desc->bytes = need;
+  desc->data = packed;
+  return W4A16_OK;
+}
+
+size_t w4a16_gemm_workspace_size(int total_slots, int E, int N, int K, int block_m) {
+  (void)total_slots;
+  (void)E;
+  (void)N;
+  (void)K;
+  if (!valid_block_m(block_m)) return 0;
+  return round_up(static_cast<size_t>(split_unit_budget(block_m)) * sizeof(int32_t), 256) +
+         kPartialBytes;
+}
+
+w4a16_status_t w4a16_workspace_clear(void* workspace, size_t workspace_bytes,
+                                     w4a16_stream_t stream) {
+  if (!workspace && workspace_bytes) return fail(W4A16_INVALID_ARG, "NULL workspace");
+  if (!workspace_bytes) return W4A16_OK;
+  cudaError_t err = cudaMemsetAsync(workspace, 0, workspace_bytes, stream);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaMemsetAsync");
+  return W4A16_OK;
+}
+
+w4a16_status_t w4a16_moe_gemm(const uint16_t* A, int64_t lda, int a_row_div,
+                              const w4a16_packed_weights_t* W, const w4a16_routing_t* routing,
+                              int epilogue, uint32_t row_flags, uint16_t* C, int64_t ldc,
+                              void* workspace, size_t workspace_bytes,
+                              int expected_rows_per_expert, const w4a16_schedule_t* schedule,
+                              int32_t* dev_err, w4a16_stream_t stream) {
+  DeviceFacts dev;
+  w4a16_status_t st = device_facts(&dev);
+  if (st != W4A16_OK) return st;
+  if (row_flags & ~(W4A16_A_ROWS_SORTED | W4A16_C_ROWS_SORTED))
+    return fail(W4A16_INVALID_ARG, "unknown row flags");
+  GemmCall c{A, lda, a_row_div, W, routing, epilogue, row_flags, C, ldc, workspace,
+             workspace_bytes, expected_rows_per_expert, schedule, dev_err, 0};
+  return run_gemm(c, dev, stream);
+}
+
+w4a16_status_t w4a16_topk_sum(const uint16_t* Y, const int32_t* topk_ids,
+                              const float* topk_weights, int T, int top_k, int H,
+                              uint16_t* out, w4a16_stream_t stream) {
+  if (T < 0 || top_k <= 0 || H <= 0 || H % 8) return fail(W4A16_INVALID_ARG, "need H %% 8 == 0");
+  if (T > 0 && (!Y || !topk_ids || !topk_weights || !out))
+    return fail(W4A16_INVALID_ARG, "NULL pointer");
+  if (reinterpret_cast<uintptr_t>(Y) % 16 || reinterpret_cast<uintptr_t>(out) % 16)
+    return fail(W4A16_INVALID_ARG, "Y and out must be 16-byte aligned");
+  DeviceFacts dev;
+  w4a16_status_t st = device_facts(&dev);
+  if (st != W4A16_OK) return st;
+  cudaError_t err = launch_topk_sum(Y, topk_ids, topk_weights, T, top_k, H, out, stream);
+  if (err != cudaSuccess) return cuda_fail(err, "topk_sum launch");
+  return W4A16_OK;
+}
+
+int w4a16_plan_block_m(int T, int top_k, int E, int E_global) {
+  if (T <= 0 || top_k <= 0 || E <= 0) return 16;
+  const int eg = E_global > 0 ? E_global : E;
+  const double rows = static_cast<double>(T) * top_k / eg;  // expected rows per local expert
+  if (rows <= 12.0) return 16;
+  if (rows <= 24.0) return 32;
+  if (rows <= 48.0) return 64;
+  return 128;
+}
+
+w4a16_status_t w4a16_plan_gemm(int total_slots, int E, int N, int K, int block_m,
+                               int expected_rows_per_expert, int num_sms, w4a16_plan_t* plan) {
+  if (!plan || total_slots < 0 || E <= 0 || num_sms <= 0)
+    return fail(W4A16_INVALID_ARG, "bad planner arguments");
+  if (!valid_block_m(block_m) || K % kBlockK || N % kTileRows || K <= 0 || N <= 0)
+    return fail(W4A16_UNSUPPORTED, "unsupported shape for the planner");
+  plan_gemm(total_slots, E, N, K, block_m, expected_rows_per_expert, num_sms, plan);
+  return W4A16_OK;
+}
+
+// Layer workspace, in order (each piece 256-byte aligned):
+//   sorted_ids [cap] | expert_ids [cap / bm] | ntp [1] | K-split counters | K-split partials |
+//   h (SiLU output, sorted rows) [cap, I] BF16 | Y (down output, slot rows) [T*top_k, H] BF16
+struct LayerLayout {
+  int block_m;
+  int64_t cap;
+  size_t off_sorted, off_expert, off_ntp, off_cnt, off_part, off_h, off_y, total;
+};
+
+static LayerLayout layer_layout(int T, int top_k, int E, int E_global, int H, int I, int block_m) {
+  LayerLayout L{};
+  L.block_m = block_m > 0 ? block_m : w4a16_plan_block_m(T, top_k, E, E_global);
+  L.cap = w4a16_align_capacity(T, top_k, E, L.block_m);
+  size_t o = 0;
+  L.off_sorted = o;
+  o = round_up(o + L.cap * 4, 256);
+  L.off_expert = o;
+  o = round_up(o + (L.cap / L.block_m) * 4, 256);
+  L.off_ntp = o;
+  o = round_up(o + 4, 256);
+  L.off_cnt = o;
+  o = round_up(o + split_unit_budget(L.block_m) * 4, 256);
+  L.off_part = o;
+  o += kPartialBytes;
+  L.off_h = o;
+  o = round_up(o + static_cast<size_t>(L.cap) * I * 2, 256);
+  L.off_y = o;
+  o = round_up(o + static_cast<size_t>(T) * top_k * H * 2, 256);
+  L.total = o;
+  return L;
+}
+
+size_t w4a16_layer_workspace_size(int T, int top_k, int E, int E_global, int H, int I,
+                                  int block_m) {
+  if (T < 0 || top_k <= 0 || E <= 0 || H <= 0 || I <= 0) return 0;
+  if (block_m != 0 && !valid_block_m(block_m)) return 0;
+  return layer_layout(T, top_k, E, E_global, H, I, block_m).total;
+}
+
+w4a16_status_t w4a16_moe_layer(const uint16_t* x, const w4a16_packed_weights_t* w13,
+                               const w4a16_packed_weights_t* w2, const int32_t* topk_ids,
+                               const float* topk_weights, int T, int top_k, int E_global,
+                               int block_m, uint16_t* out, void* workspace,
+                               size_t workspace_bytes, int32_t* dev_err, w4a16_stream_t stream) {
+  w4a16_status_t st = check_packed(w13);
+  if (st != W4A16_OK) return st;
+  if ((st = check_packed(w2)) != W4A16_OK) return st;
+  if (!(w13->flags & W4A16_PACK_GATE_UP_PAIRED))
+    return fail(W4A16_BAD_PACKED_WEIGHT, "gate_up weight must be packed with GATE_UP_PAIRED");
+  const int E = w13->E, H = w13->K, I = w13->N / 2;
+  if (w2->E != E || w2->N != H || w2->K != I)
+    return fail(W4A16_BAD_PACKED_WEIGHT, "down weight [%d,%d,%d] does not match gate_up [%d,%d,%d]",
+                w2->E, w2->N, w2->K, E, w13->N, H);
+  if (T < 0 || top_k <= 0 || E <= 0 || E > 1024 || H % 8)
+    return fail(W4A16_INVALID_ARG, "bad layer sizes");
+  if (block_m != 0 && !valid_block_m(block_m))
+    return fail(W4A16_UNSUPPORTED, "block_m %d: supported values are 16, 32, 64, 128", block_m);
+  if (T > 0 && (!x || !topk_ids || !topk_weights || !out))
+    return fail(W4A16_INVALID_ARG, "NULL pointer");
+  const LayerLayout L = layer_layout(T, top_k, E, E_global, H, I, block_m);
+  if (!workspace || workspace_bytes < L.total || reinterpret_cast<uintptr_t>(workspace) % 256)
+    return fail(W4A16_WORKSPACE_TOO_SMALL, "layer workspace needs %zu bytes, 256-byte aligned",
+                L.total);
+  DeviceFacts dev;
+  if ((st = device_facts(&dev)) != W4A16_OK) return st;
+  if (T == 0) return W4A16_OK;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* sorted_ids = reinterpret_cast<int32_t*>(ws + L.off_sorted);
+  int32_t* expert_ids = reinterpret_cast<int32_t*>(ws + L.off_expert);
+  int32_t* ntp = reinterpret_cast<int32_t*>(ws + L.off_ntp);
+  uint16_t* h = reinterpret_cast<uint16_t*>(ws + L.off_h);
+  uint16_t* y = reinterpret_cast<uint16_t*>(ws + L.off_y);
+  const int n_slots = T * top_k;
+
+  cudaError_t err = launch_moe_align(topk_ids, n_slots, E, L.block_m, sorted_ids, expert_ids, ntp,
+                                     L.cap, 0, dev_err,
+                                     reinterpret_cast<int32_t*>(ws + L.off_cnt),
+                                     static_cast<int>(split_unit_budget(L.block_m)), stream);
+  if (err != cudaSuccess) return cuda_fail(err, "moe_align launch");
+
+  w4a16_routing_t R{sorted_ids, expert_ids, ntp, L.cap, L.block_m, n_slots};
+  const int eg = E_global > 0 ? E_global : E;
+  const int rows_hint = std::max(1, static_cast<int>(std::lround(static_cast<double>(n_slots) / eg)));
+  GemmCall g1{x, H, top_k, w13, &R, W4A16_EPILOGUE_SILU_MUL, W4A16_C_ROWS_SORTED, h, I,
+              ws + L.off_cnt, (L.off_h - L.off_cnt), rows_hint, nullptr, dev_err, 0};
+  if ((st = run_gemm(g1, dev, stream)) != W4A16_OK) return st;
+  GemmCall g2{h, I, 1, w2, &R, W4A16_EPILOGUE_NONE, W4A16_A_ROWS_SORTED, y, H,
+              ws + L.off_cnt, (L.off_h - L.off_cnt), rows_hint, nullptr, dev_err, 1};
+  if ((st = run_gemm(g2, dev, stream)) != W4A16_OK) return st;
+  err = launch_topk_sum(y, topk_ids, topk_weights, T, top_k, H, out, stream);
+  if (err != cudaSuccess) return cuda_fail(err, "topk_sum launch");
+  return W4A16_OK;
+}
+
+w4a16_status_t w4a16_debug_dequant(const w4a16_packed_weights_t* W, int expert, uint16_t* out,
+                                   w4a16_stream_t stream) {
+  w4a16_status_t st = check_packed(W);
+  if (st != W4A16_OK) return st;
+  if (expert < 0 || expert >= W->E || !out) return fail(W4A16_INVALID_ARG, "bad expert or output");
+  DeviceFacts dev;
+  if ((st = device_facts(&dev)) != W4A16_OK) return st;
+  cudaError_t err = launch_debug_dequant(W->data, expert, W->N, W->K, W->flags, out, stream);
+  if (err != cudaSuccess) return cuda_fail(err, "debug_dequant launch");
+  return W4A16_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,303 @@
+// Device-side building blocks for the sm_103a kernels: mbarriers, bulk TMA,
+// cp.async, tcgen05 (TMEM allocation, MMA, loads/stores), proxy fences and
+// programmatic dependent launch.  Hand-written inline PTX; every wait is
+// bounded so a broken pipeline reports an error instead of hanging.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "w4a16_moe.h"
+
+namespace w4a16 {
+
+// ---- packed-weight geometry (shared by the packer, the GEMM and debug dequant) -----------
+constexpr int kTileRows = 128;             // weight rows per tile = MMA M
+constexpr int kBlockK = 64;                // K elements per pipeline stage
+constexpr int kCodeHalfBytes = kTileRows * 16;           // 4 words of 128 rows
+constexpr int kScaleOffset = 2 * kCodeHalfBytes;         // 4096
+constexpr int kChunkBytes = kScaleOffset + kTileRows * 4;  // 4608 bytes per (tile, kb)
+constexpr int kHeaderBytes = 256;
+
+// Device header at the start of every packed blob.
+struct PackedHeader {
+  uint64_t magic;
+  uint32_t version;
+  uint32_t flags;
+  int32_t E, N, K, group;
+  int32_t n_tiles, n_kb;
+};
+
+// Canonical weight row of tile-row r (0..127) of tile j.  Paired gate/up tiles interleave
+// 16-row groups: lanes [32w, 32w+16) of a tile hold gate rows, [32w+16, 32w+32) the up rows
+// with the same intermediate index.
+__host__ __device__ inline int tile_row_to_canonical(int j, int r, int N, bool paired) {
+  if (!paired) return j * kTileRows + r;
+  const int I = N / 2;
+  const int w = r >> 5, l = r & 31;
+  const int col = 64 * j + 16 * w + (l & 15);
+  return (l < 16) ? col : I + col;
+}
+
+// Nibble position p of a packed word holds element kPerm[p] of the canonical word, so that
+// (word >> 4m) & 0x000F000F yields elements (2m, 2m+1) in the two 16-bit halves.
+__host__ __device__ inline uint32_t interleave_nibbles(uint32_t w) {
+  uint32_t out = 0;
+  // positions 0..3 <- elements 0,2,4,6 ; positions 4..7 <- elements 1,3,5,7
+  for (int m = 0; m < 4; ++m) {
+    out |= ((w >> (8 * m)) & 0xFu) << (4 * m);
+    out |= ((w >> (8 * m + 4)) & 0xFu) << (4 * (m + 4));
+  }
+  return out;
+}
+
+// ---- small helpers --------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void set_dev_err(int32_t* dev_err, int bits) {
+  if (dev_err) atomicOr(dev_err, bits);
+}
+
+// Two BF16 weights from a packed word: bits (m, m+4) -> ((q - 8) * s) rounded once.
+// 0x4300 | q is the BF16 value 128 + q exactly; subtracting 136 leaves q - 8 exactly; the
+// product with the scale pair is one round-to-nearest-even BF16 multiply.
+__device__ __forceinline__ uint32_t dequant_pair(uint32_t shifted_word, uint32_t scale2) {
+  uint32_t v;
+  asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(v) : "r"(shifted_word), "r"(0x000F000Fu), "r"(0x43004300u));
+  uint32_t t, w;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(t) : "r"(v), "r"(0x43084308u));
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(w) : "r"(t), "r"(scale2));
+  return w;
+}
+
+// Eight dequantised pairs (16 weights, columns 4w..4w+3 for two words) from one packed word:
+// writes out[0..3] = pairs (0,1),(2,3),(4,5),(6,7) of the word's 8 elements.
+__device__ __forceinline__ void dequant_word(uint32_t word, uint32_t scale2, uint32_t* out) {
+  out[0] = dequant_pair(word, scale2);
+  out[1] = dequant_pair(word >> 4, scale2);
+  out[2] = dequant_pair(word >> 8, scale2);
+  out[3] = dequant_pair(word >> 12, scale2);
+}
+
+// Dequantise one tile row of a 64-wide K block from a chunk (shared or global memory):
+// 32 BF16x2 registers in K order (register c holds elements 2c, 2c+1).
+__device__ __forceinline__ void dequant_row64(uint4 lo, uint4 hi, uint32_t scales2x,
+                                              uint32_t (&r)[32]) {
+  const uint32_t s0 = __byte_perm(scales2x, 0, 0x1010);
+  const uint32_t s1 = __byte_perm(scales2x, 0, 0x3232);
+  dequant_word(lo.x, s0, &r[0]);
+  dequant_word(lo.y, s0, &r[4]);
+  dequant_word(lo.z, s0, &r[8]);
+  dequant_word(lo.w, s0, &r[12]);
+  dequant_word(hi.x, s1, &r[16]);
+  dequant_word(hi.y, s1, &r[20]);
+  dequant_word(hi.z, s1, &r[24]);
+  dequant_word(hi.w, s1, &r[28]);
+}
+
+// ---- mbarrier ------------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: ~2^31 cycles (about a second) before giving up.  `abort_flag` (shared) lets
+// the other roles of the CTA leave promptly once one of them has given up.
+constexpr long long kWaitLimitCycles = 1ll << 31;
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int32_t* dev_err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      *abort_flag = 1;
+      set_dev_err(dev_err, W4A16_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Wait without an abort check (teardown drains).
+__device__ __forceinline__ bool mbar_wait_plain(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  }
+  return true;
+}
+
+// ---- bulk TMA and cp.async -------------------------------------------------------------------
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// 1-D bulk copy global -> shared, completion counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// 16-byte async copy with zero fill when src_bytes == 0.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+// Arrive on `bar` once all earlier cp.async of this thread have landed (count not raised).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// ---- programmatic dependent launch --------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---- tcgen05 -------------------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16 (BF16 inputs, FP32 accumulate).
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on `bar` when every tcgen05 operation issued so far by this thread completes.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns: thread (lane l) gets columns [c, c+32) of lane l.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major operand in the 128-byte swizzle layout:
+// rows of 128 bytes (64 BF16), 8-row groups 1024 bytes apart, tile base 1024-byte aligned.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);       // start address
+  d |= static_cast<uint64_t>(1u) << 16;                      // leading byte offset (unused here)
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;              // stride byte offset: 8-row groups
+  d |= static_cast<uint64_t>(1u) << 46;                      // descriptor version
+  d |= static_cast<uint64_t>(2u) << 61;                      // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: BF16 A and B (K-major), FP32 D, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+  return (1u << 4)                                   // D format: F32
+         | (1u << 7)                                 // A format: BF16
+         | (1u << 10)                                // B format: BF16
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+}  // namespace w4a16

@@ -1,0 +1,39 @@
+// Arguments of the indexed GEMM kernel, shared by the launcher and the C ABI layer.
+#pragma once
+
+#include "common.cuh"
+
+namespace w4a16 {
+
+struct GemmArgs {
+  const uint16_t* A;
+  int64_t lda;
+  int a_row_div;
+  int a_sorted;
+  const uint8_t* wblob;
+  int E, N, K, n_tiles, n_kb;
+  int paired;
+  const int32_t* sorted_ids;
+  const int32_t* expert_ids;
+  const int32_t* ntp;
+  int block_m;
+  int total_slots;
+  int64_t capacity;
+  int epilogue;
+  int c_sorted;
+  uint16_t* C;
+  int64_t ldc;
+  float* part;
+  int32_t* cnt;
+  int split_k;
+  int64_t max_split_units;  // K splits are reduced on the device until units fit the scratch
+  int32_t* dev_err;
+  int evict_first;
+  int routing_ready;  // routing was complete before the previous kernel started
+};
+
+cudaError_t launch_gemm(const GemmArgs& args, int grid, bool pdl, cudaStream_t stream);
+void plan_gemm(int total_slots, int E, int N, int K, int block_m, int rows_per_expert,
+               int num_sms, w4a16_plan_t* plan);
+
+}  // namespace w4a16

@@ -1,0 +1,90 @@
+// Offline weight repack and the debug dequantiser.
+//
+// "vLLM x Novita AI: Chord, Faster INT4 MoE for Kimi K2.x", "Grouped SM90 kernels": weights
+// are repacked once for the kernel that reads them and the prepared weight records its mode.
+// Here the target is the GB300 GEMM's stream of 4608-byte chunks, one per (expert, 128-row
+// tile, 64-wide K block), read by one bulk copy each:
+//   bytes [0, 2048)     row r at 16*r: canonical words 0..3 of the block (K 0..31)
+//   bytes [2048, 4096)  row r at 2048 + 16*r: words 4..7 (K 32..63)
+//   bytes [4096, 4608)  row r at 4096 + 4*r: the two BF16 scales of the block
+// Words are nibble-interleaved (positions 0..3 hold elements 0,2,4,6 and 4..7 hold 1,3,5,7)
+// so that one mask yields two neighbouring elements in the two halves of a register.
+#include "common.cuh"
+
+namespace w4a16 {
+
+// One thread per tile row; grid (n_kb, n_tiles, E).
+__global__ void __launch_bounds__(kTileRows)
+    pack_kernel(const int32_t* __restrict__ qweight, const uint16_t* __restrict__ scales, int N,
+                int K, int n_tiles, int n_kb, int paired, uint8_t* __restrict__ out) {
+  const int kb = blockIdx.x, j = blockIdx.y, e = blockIdx.z, r = threadIdx.x;
+  const int n = tile_row_to_canonical(j, r, N, paired != 0);
+  const int64_t row = static_cast<int64_t>(e) * N + n;
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(qweight) + row * (K / 8) + kb * 8;
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = interleave_nibbles(__ldg(src + i));
+  const uint16_t* s = scales + row * (K / 32) + kb * 2;
+  const uint32_t s2 = static_cast<uint32_t>(__ldg(s)) | (static_cast<uint32_t>(__ldg(s + 1)) << 16);
+  uint8_t* chunk =
+      out + kHeaderBytes + ((static_cast<int64_t>(e) * n_tiles + j) * n_kb + kb) * kChunkBytes;
+  reinterpret_cast<uint4*>(chunk)[r] = make_uint4(w[0], w[1], w[2], w[3]);
+  reinterpret_cast<uint4*>(chunk + kCodeHalfBytes)[r] = make_uint4(w[4], w[5], w[6], w[7]);
+  reinterpret_cast<uint32_t*>(chunk + kScaleOffset)[r] = s2;
+}
+
+__global__ void write_header_kernel(PackedHeader h, uint8_t* out) {
+  *reinterpret_cast<PackedHeader*>(out) = h;
+}
+
+// Debug: dequantise expert e back to canonical [N, K] with the GEMM's conversion routine.
+__global__ void __launch_bounds__(kTileRows)
+    debug_dequant_kernel(const uint8_t* __restrict__ packed, int e, int N, int K, int n_tiles,
+                         int n_kb, int paired, uint16_t* __restrict__ out) {
+  const int kb = blockIdx.x, j = blockIdx.y, r = threadIdx.x;
+  const uint8_t* chunk =
+      packed + kHeaderBytes + ((static_cast<int64_t>(e) * n_tiles + j) * n_kb + kb) * kChunkBytes;
+  const uint4 lo = reinterpret_cast<const uint4*>(chunk)[r];
+  const uint4 hi = reinterpret_cast<const uint4*>(chunk + kCodeHalfBytes)[r];
+  const uint32_t s2 = reinterpret_cast<const uint32_t*>(chunk + kScaleOffset)[r];
+  uint32_t v[32];
+  dequant_row64(lo, hi, s2, v);
+  const int n = tile_row_to_canonical(j, r, N, paired != 0);
+  uint4* dst = reinterpret_cast<uint4*>(out + static_cast<int64_t>(n) * K + kb * kBlockK);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) dst[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+
+cudaError_t launch_pack(const int32_t* qweight, const uint16_t* scales, int E, int N, int K,
+                        uint32_t flags, void* packed, cudaStream_t stream) {
+  const int n_tiles = N / kTileRows, n_kb = K / kBlockK;
+  PackedHeader h{};
+  h.magic = W4A16_PACK_MAGIC;
+  h.version = W4A16_PACK_VERSION;
+  h.flags = flags;
+  h.E = E;
+  h.N = N;
+  h.K = K;
+  h.group = 32;
+  h.n_tiles = n_tiles;
+  h.n_kb = n_kb;
+  uint8_t* out = static_cast<uint8_t*>(packed);
+  write_header_kernel<<<1, 1, 0, stream>>>(h, out);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  if (E == 0) return cudaSuccess;
+  pack_kernel<<<dim3(n_kb, n_tiles, E), kTileRows, 0, stream>>>(
+      qweight, scales, N, K, n_tiles, n_kb, (flags & W4A16_PACK_GATE_UP_PAIRED) ? 1 : 0, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_dequant(const void* packed, int e, int N, int K, uint32_t flags,
+                                 uint16_t* out, cudaStream_t stream) {
+  const int n_tiles = N / kTileRows, n_kb = K / kBlockK;
+  debug_dequant_kernel<<<dim3(n_kb, n_tiles), kTileRows, 0, stream>>>(
+      static_cast<const uint8_t*>(packed), e, N, K, n_tiles, n_kb,
+      (flags & W4A16_PACK_GATE_UP_PAIRED) ? 1 : 0, out);
+  return cudaGetLastError();
+}
+
+}  // namespace w4a16
