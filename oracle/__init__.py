@@ -59,7 +59,7 @@ def lib():
                 "w4a16_oracle_dequant": (None, [vp, vp, i64, i32, i32, vp]),
                 "w4a16_oracle_gemm_rows": (None, [vp, i32, i32, vp, vp, i32, i32, vp, vp, i64, vp]),
                 "w4a16_oracle_moe_gemm": (i32, [vp, i32, i32, vp, vp, i32, i32, vp, vp, i32, i32,
-                                                i32, i32, i32, vp]),
+                                                i32, i32, i32, vp, vp]),
                 "w4a16_oracle_silu_mul": (None, [vp, i64, i32, vp]),
                 "w4a16_oracle_topk_sum": (None, [vp, vp, vp, i32, i32, i32, vp]),
                 "w4a16_oracle_moe_layer": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
@@ -158,8 +158,9 @@ def gemm_rows(A, a_row_div: int, qweight, scales, slots, experts, group: int = 3
 
 
 def moe_gemm(A, a_row_div: int, qweight, scales, sorted_ids, expert_ids, ntp: int, block_m: int,
-             total_slots: int, group: int = 32, threads: int = 1, out=None) -> torch.Tensor:
-    """Indexed grouped GEMM; returns C bf16 [total_slots, N] (unrouted rows are 0).
+             total_slots: int, group: int = 32, threads: int = 1, out_f32: bool = False) -> torch.Tensor:
+    """Indexed grouped GEMM; returns C [total_slots, N] (unrouted rows are 0), BF16, or
+    the unrounded FP32 sums with ``out_f32``.
 
     With ``threads > 1`` the same single-threaded function runs over disjoint
     expert ranges on that many host threads; every output element has the
@@ -172,12 +173,13 @@ def moe_gemm(A, a_row_div: int, qweight, scales, sorted_ids, expert_ids, ntp: in
     ei = _np(expert_ids, np.int32)
     K = a.shape[-1]
     E, N = q.shape[0], q.shape[1]
-    C = np.zeros((total_slots, N), np.uint16) if out is None else out
+    C = np.zeros((total_slots, N), np.float32 if out_f32 else np.uint16)
     L = lib()
 
     def run(lo, hi):
         rc = L.w4a16_oracle_moe_gemm(_ptr(a), a_row_div, K, _ptr(q), _ptr(s), N, group, _ptr(si),
-                                     _ptr(ei), ntp, block_m, total_slots, lo, hi, _ptr(C))
+                                     _ptr(ei), ntp, block_m, total_slots, lo, hi,
+                                     None if out_f32 else _ptr(C), _ptr(C) if out_f32 else None)
         if rc:
             raise ValueError(f"oracle moe_gemm failed with code {rc}")
 
@@ -192,7 +194,7 @@ def moe_gemm(A, a_row_div: int, qweight, scales, sorted_ids, expert_ids, ntp: in
         bounds = sorted(set(min(max(b, 0), E) for b in bounds))
         with ThreadPoolExecutor(len(bounds) - 1) as ex:
             list(ex.map(lambda lh: run(*lh), zip(bounds[:-1], bounds[1:])))
-    return _bf16_tensor(C)
+    return torch.from_numpy(C) if out_f32 else _bf16_tensor(C)
 
 
 def silu_mul(C) -> torch.Tensor:
@@ -204,7 +206,10 @@ def silu_mul(C) -> torch.Tensor:
 
 
 def topk_sum(Y, topk_ids, topk_weights) -> torch.Tensor:
-    y = _np(Y, np.uint16)
+    """Y fp32 [T*k, H] (per-slot down outputs) -> bf16 [T, H]."""
+    if isinstance(Y, torch.Tensor) and Y.dtype == torch.bfloat16:
+        Y = Y.float()
+    y = _np(Y, np.float32)
     ids = _np(topk_ids, np.int32)
     w = _np(topk_weights, np.float32)
     T, k = ids.shape
@@ -243,5 +248,6 @@ def moe_layer_parallel(x, w13_q, w13_s, w2_q, w2_s, topk_ids, topk_weights, bloc
     sorted_ids, expert_ids, ntp = moe_align(ids, E, block_m)
     c13 = moe_gemm(x, k, w13_q, w13_s, sorted_ids, expert_ids, ntp, block_m, T * k, threads=threads)
     h = silu_mul(c13)
-    y = moe_gemm(h, 1, w2_q, w2_s, sorted_ids, expert_ids, ntp, block_m, T * k, threads=threads)
+    y = moe_gemm(h, 1, w2_q, w2_s, sorted_ids, expert_ids, ntp, block_m, T * k, threads=threads,
+                 out_f32=True)
     return topk_sum(y, ids, topk_weights)

@@ -31,7 +31,12 @@
 //    BF16 gate_up output; evaluated in double, rounded once to BF16.
 //  * topk_sum -- out[t, :] = sum over valid slots s (ascending) of
 //    topk_weights[t, s] * Y[t*top_k + s, :]; double, rounded once to BF16.
-//  * layer -- align, gate_up gemm, silu_mul, down gemm, topk_sum in that
+//    The per-slot down outputs Y stay FP32 (the pages fix no precision for
+//    them; rounding them to BF16 first would add up to half a BF16 ulp of the
+//    largest per-slot value, an error as large as the stated output
+//    tolerance, so the reading that fits that tolerance keeps them in FP32).
+//  * layer -- align, gate_up gemm (BF16 out), silu_mul, down gemm (FP32 out),
+//    topk_sum in that
 //    order (Chord page, "Measurements": the per-layer time is gate_up plus
 //    down; "humans& ..." page: FC1, FC2 and the top-K merge).
 //
@@ -103,9 +108,10 @@ float dequant_one(const int32_t* qrow, const uint16_t* srow, int k, int group) {
   return bf16_to_float(float_to_bf16(prod));
 }
 
-// C[row] for one (slot, expert) pair: FP32 dot over k ascending, BF16 out.
+// C[row] for one (slot, expert) pair: FP32 dot over k ascending, BF16 out (or the FP32
+// sum itself when out_f32 is given).
 void gemm_one_row(const uint16_t* a, int K, const int32_t* qweight, const uint16_t* scales,
-                  int N, int group, int e, uint16_t* out_row) {
+                  int N, int group, int e, uint16_t* out_row, float* out_f32 = nullptr) {
   for (int n = 0; n < N; ++n) {
     const int32_t* qrow = qweight + (static_cast<int64_t>(e) * N + n) * (K / 8);
     const uint16_t* srow = scales + (static_cast<int64_t>(e) * N + n) * (K / group);
@@ -114,7 +120,10 @@ void gemm_one_row(const uint16_t* a, int K, const int32_t* qweight, const uint16
       const float p = bf16_to_float(a[k]) * dequant_one(qrow, srow, k, group);
       acc = acc + p;
     }
-    out_row[n] = float_to_bf16(acc);
+    if (out_f32)
+      out_f32[n] = acc;
+    else
+      out_row[n] = float_to_bf16(acc);
   }
 }
 
@@ -201,10 +210,11 @@ void w4a16_oracle_gemm_rows(const uint16_t* A, int a_row_div, int K, const int32
 
 // Indexed grouped GEMM over the aligned routing.  Writes C[i, :] for every
 // routed slot i whose expert lies in [e_lo, e_hi); other rows are untouched.
+// C is BF16, or FP32 (the unrounded sums) when C_f32 is not NULL.
 int w4a16_oracle_moe_gemm(const uint16_t* A, int a_row_div, int K, const int32_t* qweight,
                           const uint16_t* scales, int N, int group, const int32_t* sorted_ids,
                           const int32_t* expert_ids, int num_tokens_padded, int block_m,
-                          int total_slots, int e_lo, int e_hi, uint16_t* C) {
+                          int total_slots, int e_lo, int e_hi, uint16_t* C, float* C_f32) {
   if (a_row_div <= 0 || K % 8 || K % group || block_m <= 0) return -3;
   for (int64_t p = 0; p < num_tokens_padded; ++p) {
     const int32_t i = sorted_ids[p];
@@ -212,7 +222,9 @@ int w4a16_oracle_moe_gemm(const uint16_t* A, int a_row_div, int K, const int32_t
     const int32_t e = expert_ids[p / block_m];
     if (e < e_lo || e >= e_hi) continue;
     const uint16_t* a = A + static_cast<int64_t>(i / a_row_div) * K;
-    gemm_one_row(a, K, qweight, scales, N, group, e, C + static_cast<int64_t>(i) * N);
+    const int64_t row = static_cast<int64_t>(i) * N;
+    gemm_one_row(a, K, qweight, scales, N, group, e, C_f32 ? nullptr : C + row,
+                 C_f32 ? C_f32 + row : nullptr);
   }
   return 0;
 }
@@ -231,8 +243,8 @@ void w4a16_oracle_silu_mul(const uint16_t* C, int64_t rows, int I, uint16_t* h) 
   }
 }
 
-// Y bf16 [T*top_k, H] -> out bf16 [T, H]; slots with id -1 are skipped.
-void w4a16_oracle_topk_sum(const uint16_t* Y, const int32_t* topk_ids, const float* topk_weights,
+// Y fp32 [T*top_k, H] -> out bf16 [T, H]; slots with id -1 are skipped.
+void w4a16_oracle_topk_sum(const float* Y, const int32_t* topk_ids, const float* topk_weights,
                            int T, int top_k, int H, uint16_t* out) {
   for (int64_t t = 0; t < T; ++t) {
     for (int c = 0; c < H; ++c) {
@@ -240,7 +252,7 @@ void w4a16_oracle_topk_sum(const uint16_t* Y, const int32_t* topk_ids, const flo
       for (int s = 0; s < top_k; ++s) {
         const int64_t i = t * top_k + s;
         if (topk_ids[i] < 0) continue;
-        acc += static_cast<double>(topk_weights[i]) * bf16_to_float(Y[i * H + c]);
+        acc += static_cast<double>(topk_weights[i]) * static_cast<double>(Y[i * H + c]);
       }
       out[t * H + c] = double_to_bf16(acc);
     }
@@ -260,15 +272,16 @@ int w4a16_oracle_moe_layer(const uint16_t* x, const int32_t* w13_q, const uint16
   int rc = w4a16_oracle_align(topk_ids, T, top_k, E, block_m, cap, sorted_ids.data(),
                               expert_ids.data(), &ntp);
   if (rc) return rc;
-  std::vector<uint16_t> c13(slots * 2 * I, 0), h(slots * I, 0), y(slots * H, 0);
+  std::vector<uint16_t> c13(slots * 2 * I, 0), h(slots * I, 0);
+  std::vector<float> y(slots * H, 0.0f);
   rc = w4a16_oracle_moe_gemm(x, top_k, H, w13_q, w13_s, 2 * I, group, sorted_ids.data(),
                              expert_ids.data(), ntp, block_m, static_cast<int>(slots), 0, E,
-                             c13.data());
+                             c13.data(), nullptr);
   if (rc) return rc;
   w4a16_oracle_silu_mul(c13.data(), slots, I, h.data());
   rc = w4a16_oracle_moe_gemm(h.data(), 1, I, w2_q, w2_s, H, group, sorted_ids.data(),
                              expert_ids.data(), ntp, block_m, static_cast<int>(slots), 0, E,
-                             y.data());
+                             nullptr, y.data());
   if (rc) return rc;
   w4a16_oracle_topk_sum(y.data(), topk_ids, topk_weights, T, top_k, H, out);
   return 0;

@@ -329,6 +329,16 @@ def test_gemm_rows_matches_indexed_gemm():
     assert torch.equal(bits_t(rows), bits_t(C))
 
 
+def test_gemm_fp32_output_rounds_to_the_bf16_output():
+    qw, sc, x, ids, _ = _tiny_problem(19)
+    T, k = ids.shape
+    s, e, ntp = oracle.moe_align(ids, 4, 4)
+    c16 = oracle.moe_gemm(x, k, qw, sc, s, e, ntp, 4, T * k)
+    c32 = oracle.moe_gemm(x, k, qw, sc, s, e, ntp, 4, T * k, out_f32=True)
+    assert c32.dtype == torch.float32
+    assert torch.equal(bits_t(c32.to(torch.bfloat16)), bits_t(c16))
+
+
 def test_gemm_threaded_partition_is_identical():
     qw, sc, x, ids, _ = _tiny_problem(17, T=30, E=4)
     T, k = ids.shape
@@ -408,7 +418,8 @@ def _round_bf16_exact(v: Fraction) -> float:
 # ---- whole layer --------------------------------------------------------------------
 
 def _layer_brute(inp):
-    """Per-token loops in numpy float64 with BF16 rounding at the stage boundaries."""
+    """Per-token loops in numpy float64, BF16 rounding at the gate_up, SiLU-mul and final
+    outputs (the per-slot down outputs are summed unrounded)."""
     from scipy.special import expit
     wl = inp.wl
     w13 = dequant_np(inp.w13_q.numpy(), inp.w13_s.view(torch.int16).numpy())
@@ -429,7 +440,7 @@ def _layer_brute(inp):
             c = rb(w13[ex] @ xa[t])
             g, u = c[: wl.I], c[wl.I:]
             h = rb(g * expit(g) * u)
-            y = rb(w2[ex] @ h)
+            y = w2[ex] @ h  # per-slot down output stays unrounded until the weighted sum
             acc += float(inp.topk_weights[t, s]) * y
         out[t] = rb(acc)
     return out
