@@ -1,0 +1,437 @@
+"""Benchmark of the W4A16 MoE expert path on GB300 (one JSON line on rank 0).
+
+Workload: Qwen3-30B-A3B-shaped experts (128 experts, top-8, hidden 2048,
+gate_up [128, 1536, 2048], down [128, 2048, 768], uint4 group-32 BF16 scales),
+seeded synthetic inputs, token sweep T in {1, 8, 64, 512, 4096}.
+
+One step = one pass of the whole path for every T of the sweep: align, gate_up
+with fused SiLU-and-mul, down, top-k weighted sum, each a C-ABI call on the
+current stream with CUDA events between them.  L2 is flushed (a 512 MB memset,
+outside the events) before every T, so weights and activations come from HBM.
+
+value = weight HBM GB/s over the sweep: sum of the packed weight bytes the two
+projections must read (experts with at least one routed row) divided by the sum
+of the gate_up and down kernel times.  The roofline object describes the GEMM
+kernel (both projections): algorithmic bytes (weights + activations in + outputs)
+per launch over its event-timed duration, against the measured HBM copy peak.
+
+--impl reference times the CPU oracle (single-threaded C++) on a bounded sample
+of the same workload and reports the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+WORKLOAD = "qwen3_30b_a3b"
+METRIC = "µs/call and weight HBM GB/s (% roofline) for W4A16 MoE gate_up+down on 1 GB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+# ---- per-T algorithmic accounting -----------------------------------------------------------
+
+def accounting(wl, T, topk_ids):
+    """Algorithmic bytes and flops of one layer call (routed rows only, no padding)."""
+    ids = topk_ids.reshape(-1)
+    valid = ids[ids >= 0]
+    T_r = int(valid.numel())
+    e_act = int(torch.unique(valid).numel())
+    tok_with_local = int((topk_ids >= 0).any(dim=1).sum())
+    H, I = wl.H, wl.I
+    w_gu = e_act * (2 * I) * H * 9 // 16  # 0.5 B per code + 2 B per 32 codes
+    w_dn = e_act * H * I * 9 // 16
+    gu = {"weight_bytes": w_gu, "act_bytes": tok_with_local * H * 2, "out_bytes": T_r * I * 2,
+          "flops": 2 * T_r * (2 * I) * H}
+    dn = {"weight_bytes": w_dn, "act_bytes": T_r * I * 2, "out_bytes": T_r * H * 4,
+          "flops": 2 * T_r * H * I}
+    for d in (gu, dn):
+        d["bytes"] = d["weight_bytes"] + d["act_bytes"] + d["out_bytes"]
+    return {"T": T, "T_r": T_r, "E_act": e_act, "gate_up": gu, "down": dn}
+
+
+# ---- clock sampling -------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t is not None:
+            self._t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---- our arm --------------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    import w4a16_moe_expert_gb300 as lib
+    from w4a16_moe_expert_gb300 import workloads
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    lib.load()
+    wl = workloads.WORKLOADS[args.workload]
+    tokens = [int(t) for t in args.tokens.split(",")] if args.tokens else list(wl.tokens)
+    peaks, peak_src = load_peaks()
+
+    w13_q, w13_s, w2_q, w2_s = workloads.draw_layer_weights(wl)
+    w13 = lib.pack_weights(w13_q.to(dev), w13_s.to(dev), paired=True)
+    w2 = lib.pack_weights(w2_q.to(dev), w2_s.to(dev))
+    del w13_q, w13_s, w2_q, w2_s
+
+    cases = []
+    for T in tokens:
+        x, ids, w = workloads.draw_layer_routing(wl, T)
+        bm = lib.plan_block_m(T, wl.top_k, wl.E, wl.E_global)
+        cap = lib.align_capacity(T, wl.top_k, wl.E, bm)
+        case = {
+            "T": T, "block_m": bm, "cap": cap, "acct": accounting(wl, T, ids),
+            "x": x.to(dev), "ids": ids.to(dev), "w": w.to(dev),
+            "x_h": x.pin_memory(), "ids_h": ids.pin_memory(), "w_h": w.pin_memory(),
+            "sorted": torch.empty(cap, dtype=torch.int32, device=dev),
+            "expert": torch.empty(cap // bm, dtype=torch.int32, device=dev),
+            "ntp": torch.empty(1, dtype=torch.int32, device=dev),
+            "h": torch.empty((cap, wl.I), dtype=torch.bfloat16, device=dev),
+            "y": torch.empty((T * wl.top_k, wl.H), dtype=torch.float32, device=dev),
+            "out": torch.empty((T, wl.H), dtype=torch.bfloat16, device=dev),
+            "out_h": torch.empty((T, wl.H), dtype=torch.bfloat16).pin_memory(),
+            "ws": lib.gemm_workspace(T * wl.top_k, wl.E, 2 * wl.I, wl.H, bm, dev),
+            "layer_ws": torch.empty(lib.layer_workspace_size(T, wl.top_k, wl.E, wl.H, wl.I,
+                                                             wl.E_global, bm),
+                                    dtype=torch.uint8, device=dev),
+        }
+        case["routing"] = lib.Routing(case["sorted"], case["expert"], case["ntp"], bm, T * wl.top_k)
+        cases.append(case)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    rows_hint = {c["T"]: max(1, round(c["T"] * wl.top_k / wl.E_global)) for c in cases}
+
+    def path(c, ev=None):
+        """One pass of the path for one T through the C ABI (events between stages)."""
+        r = c["routing"]
+        if ev:
+            ev[0].record()
+        lib.load().w4a16_moe_align(
+            lib._ptr(c["ids"]), c["T"], wl.top_k, wl.E, c["block_m"], lib._ptr(c["sorted"]),
+            lib._ptr(c["expert"]), lib._ptr(c["ntp"]), c["cap"], 0, None, lib._stream())
+        if ev:
+            ev[1].record()
+        lib.moe_gemm(c["x"], wl.top_k, w13, r, epilogue=lib.EPILOGUE_SILU_MUL,
+                     row_flags=lib.C_ROWS_SORTED, out=c["h"], workspace=c["ws"],
+                     expected_rows_per_expert=rows_hint[c["T"]])
+        if ev:
+            ev[2].record()
+        lib.moe_gemm(c["h"], 1, w2, r, row_flags=lib.A_ROWS_SORTED | lib.C_FP32, out=c["y"],
+                     workspace=c["ws"], expected_rows_per_expert=rows_hint[c["T"]])
+        if ev:
+            ev[3].record()
+        lib.topk_sum(c["y"], c["ids"], c["w"], out=c["out"])
+        if ev:
+            ev[4].record()
+
+    def step(events=None):
+        for i, c in enumerate(cases):
+            flush.zero_()
+            path(c, events[i] if events else None)
+
+    # warm-up
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # timed region: device time from events, barrier + synchronize on both sides
+    all_events = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in cases]
+                  for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        step(all_events[s])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+
+    # per-T stage times (mean over steps, microseconds)
+    stage_us = []
+    for i, c in enumerate(cases):
+        acc = np.zeros(4)
+        for s in range(args.steps):
+            ev = all_events[s][i]
+            acc += [ev[j].elapsed_time(ev[j + 1]) * 1e3 for j in range(4)]
+        stage_us.append(acc / args.steps)
+    step_ms = float(sum(u.sum() for u in stage_us)) / 1e3
+
+    # e2e through the public layer call, host buffers, copies inside the timed region
+    e2e_events = []
+    h2d = sum(c["x_h"].numel() * 2 + c["ids_h"].numel() * 4 + c["w_h"].numel() * 4 for c in cases)
+    d2h = sum(c["out_h"].numel() * 2 for c in cases)
+    for s in range(args.warmup + args.steps):
+        evs = []
+        for c in cases:
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            c["x"].copy_(c["x_h"], non_blocking=True)
+            c["ids"].copy_(c["ids_h"], non_blocking=True)
+            c["w"].copy_(c["w_h"], non_blocking=True)
+            lib.moe_layer(c["x"], w13, w2, c["ids"], c["w"], E_global=wl.E_global,
+                          block_m=c["block_m"], out=c["out"], workspace=c["layer_ws"])
+            c["out_h"].copy_(c["out"], non_blocking=True)
+            e1.record()
+            evs.append((e0, e1))
+        if s >= args.warmup:
+            e2e_events.append(evs)
+    torch.cuda.synchronize()
+    e2e_us = [statistics.fmean(evs[i][0].elapsed_time(evs[i][1]) * 1e3 for evs in e2e_events)
+              for i in range(len(cases))]
+
+    # aggregate metric and roofline
+    w_bytes = sum(c["acct"]["gate_up"]["weight_bytes"] + c["acct"]["down"]["weight_bytes"] for c in cases)
+    gemm_us = sum(u[1] + u[2] for u in stage_us)
+    alg_bytes = sum(c["acct"]["gate_up"]["bytes"] + c["acct"]["down"]["bytes"] for c in cases)
+    hbm = float(peaks["hbm_gbs"])
+    tflops_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+
+    # max over ranks of the timed device time; value sums the ranks' work
+    t_dev = torch.tensor([gemm_us, step_ms, wall], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t_dev, op=torch.distributed.ReduceOp.MAX)
+    gemm_us_max, step_ms_max = float(t_dev[0]), float(t_dev[1])
+    value = w_bytes * world / (gemm_us_max * 1e-6) / 1e9
+    achieved = alg_bytes / (gemm_us_max * 1e-6) / 1e9
+    e2e_value = w_bytes * world / (sum(e2e_us) * 1e-6) / 1e9
+
+    sweep = []
+    for c, u, e in zip(cases, stage_us, e2e_us):
+        a = c["acct"]
+        row = {"T": c["T"], "T_r": a["T_r"], "E_act": a["E_act"], "block_m": c["block_m"],
+               "align_us": round(u[0], 2), "gate_up_us": round(u[1], 2), "down_us": round(u[2], 2),
+               "topk_sum_us": round(u[3], 2), "gate_up_plus_down_us": round(u[1] + u[2], 2),
+               "layer_e2e_us": round(e, 2)}
+        for name, t_us in (("gate_up", u[1]), ("down", u[2])):
+            d = a[name]
+            roof_us = max(d["bytes"] / (hbm * 1e9), d["flops"] / (tflops_peak * 1e12)) * 1e6
+            row[f"{name}_weight_GBps"] = round(d["weight_bytes"] / (t_us * 1e-6) / 1e9, 1)
+            row[f"{name}_TFLOPs"] = round(d["flops"] / (t_us * 1e-6) / 1e12, 2)
+            row[f"{name}_roofline_frac"] = round(roof_us / t_us, 3)
+        sweep.append(row)
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms_max, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded uint4 codes, BF16 scales in [0.005,0.02], N(0,1) BF16 "
+                "activations, softmax top-8 routing)",
+        "config": {
+            "workload": f"{wl.name}: {wl.E} experts, top-{wl.top_k}, hidden {wl.H}, "
+                        f"gate_up [{wl.E},{2 * wl.I},{wl.H}], down [{wl.E},{wl.H},{wl.I}], "
+                        f"uint4 group-32 BF16 scales",
+            "tokens": tokens,
+            "l2": "flushed by a 512 MB memset before every T (outside the timed events)",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "sweep": sweep,
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "moe_gemm_kernel (gate_up + down launches)",
+            "achieved": round(achieved, 1),
+            "peak": hbm,
+            "unit": "GB/s",
+            "frac": round(achieved / hbm, 4),
+            "peak_source": f"hbm_gbs of {peak_src}",
+            "traffic": None,
+        },
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": 4 * len(cases) * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
+    return line
+
+
+# ---- CPU oracle (baseline and reference arm) --------------------------------------------------
+
+def oracle_sample(wl, budget_s):
+    """Single-threaded oracle layer calls over the smallest T of the sweep until the budget."""
+    import oracle
+    from w4a16_moe_expert_gb300 import workloads
+
+    w = workloads.draw_layer_weights(wl)
+    done_bytes, done_s, Ts = 0, 0.0, []
+    for T in wl.tokens:
+        x, ids, tw = workloads.draw_layer_routing(wl, T)
+        est = done_s * (T * wl.top_k) / max(1, sum(t * wl.top_k for t in Ts)) if Ts else 0.0
+        if Ts and done_s + est > budget_s:
+            break
+        a = accounting(wl, T, ids)
+        t0 = time.perf_counter()
+        oracle.moe_layer(x, *w, ids, tw, block_m=16)
+        done_s += time.perf_counter() - t0
+        done_bytes += a["gate_up"]["weight_bytes"] + a["down"]["weight_bytes"]
+        Ts.append(T)
+    return done_bytes, done_s, Ts
+
+
+def cpu_baseline(wl, budget_s=15.0):
+    b, s, Ts = oracle_sample(wl, budget_s)
+    return {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"single-threaded C++ oracle, whole layer at T in {Ts} "
+                      f"({s:.1f} s of CPU work; weight bytes of those calls / time)"}
+
+
+def run_reference(args, rank, world, local_rank):
+    from w4a16_moe_expert_gb300 import workloads
+
+    wl = workloads.WORKLOADS[args.workload]
+    times, bytes_ = [], 0
+    for i in range(args.warmup + args.steps):
+        b, s, Ts = oracle_sample(wl, budget_s=args.ref_step_budget)
+        if i >= args.warmup:
+            times.append(s)
+            bytes_ = b
+    mean_s = statistics.fmean(times)
+    value = bytes_ / mean_s / 1e9
+    sample = (f"single-threaded C++ oracle, whole layer at T in {Ts} per step "
+              f"(the oracle as written; weight bytes / time)")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(mean_s * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (same seeded inputs as the CUDA arm)",
+        "config": {"workload": f"{wl.name}: {wl.E} experts, top-{wl.top_k}, hidden {wl.H}, "
+                               f"gate_up [{wl.E},{2 * wl.I},{wl.H}], down [{wl.E},{wl.H},{wl.I}], "
+                               f"uint4 group-32 BF16 scales", "tokens": Ts},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--tokens", default="", help="comma-separated subset of the token sweep")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
+    ap.add_argument("--ref-step-budget", type=float, default=4.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps are required")
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world, local_rank)), flush=True)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

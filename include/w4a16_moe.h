@@ -128,7 +128,8 @@ w4a16_status_t w4a16_pack_weights(const int32_t* qweight, const uint16_t* scales
  *     C[row_c(p), :] = A[row_a(p), :] . dequant(W[e])^T      (FP32 accumulation, BF16 out)
  * row_a(p) = i / a_row_div (top_k for gate_up, 1 for down), or p with W4A16_A_ROWS_SORTED;
  * row_c(p) = i, or p with W4A16_C_ROWS_SORTED (then padding rows p are written too, as
- * zeros).  Rows of C not named are left untouched.
+ * zeros).  Rows of C not named are left untouched.  With W4A16_C_FP32 (epilogue NONE only)
+ * C holds the FP32 sums unrounded (float, row stride ldc elements).
  * A  device BF16 [rows, K] with row stride lda elements (lda % 8 == 0, 16-byte aligned rows).
  * C  device BF16 with row stride ldc elements; N columns (epilogue NONE) or N/2 columns
  *    (epilogue SILU_MUL: C[., j] = bf16(silu(g) * u), g and u the BF16-rounded gate and up
@@ -144,6 +145,7 @@ w4a16_status_t w4a16_pack_weights(const int32_t* qweight, const uint16_t* scales
 #define W4A16_EPILOGUE_SILU_MUL 1
 #define W4A16_A_ROWS_SORTED 0x1u
 #define W4A16_C_ROWS_SORTED 0x2u
+#define W4A16_C_FP32 0x4u
 
 typedef struct {
   const int32_t* sorted_ids;        /* device [capacity] */
@@ -172,11 +174,11 @@ w4a16_status_t w4a16_moe_gemm(const uint16_t* A, int64_t lda, int a_row_div,
 
 /* ------------------------------------------------------------------------------------------
  * Top-k weighted sum (the "top-K expert output merge" of the humans& page).
- * Y device BF16 [T*top_k, H]; out[t, :] = bf16(sum over s ascending with topk_ids[t,s] >= 0
- * of topk_weights[t,s] * Y[t*top_k + s, :]), FP32 accumulation; rows of dropped slots are
- * not read.  H % 8 == 0.
+ * Y device FP32 [T*top_k, H] (the per-slot down outputs, unrounded); out[t, :] =
+ * bf16(sum over s ascending with topk_ids[t,s] >= 0 of topk_weights[t,s] * Y[t*top_k + s, :]),
+ * FP32 accumulation; rows of dropped slots are not read.  H % 8 == 0.
  * ---------------------------------------------------------------------------------------- */
-w4a16_status_t w4a16_topk_sum(const uint16_t* Y, const int32_t* topk_ids,
+w4a16_status_t w4a16_topk_sum(const float* Y, const int32_t* topk_ids,
                               const float* topk_weights, int T, int top_k, int H,
                               uint16_t* out, w4a16_stream_t stream);
 

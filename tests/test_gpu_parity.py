@@ -245,12 +245,24 @@ def test_dev_err_stays_clear_and_bad_descriptors_rejected(lib):
         lib.moe_gemm(x.to(DEV), 2, W, r, epilogue=lib.EPILOGUE_SILU_MUL)
 
 
+def test_gemm_fp32_output_mode(lib):
+    qw, sc, x, ids, W, r, (s, e, ntp) = _gemm_case(lib, 24, 4, 8, 384, 512, 32, 61)
+    ref = oracle.moe_gemm(x, 4, qw, sc, s, e, ntp, 32, 96, out_f32=True)
+    C = lib.moe_gemm(x.to(DEV), 4, W, r, row_flags=lib.C_FP32)
+    assert C.dtype == torch.float32
+    rows = routed_rows(ids)
+    g, rf = C.cpu()[rows], ref[rows]
+    rms = float(rf.pow(2).mean().sqrt())
+    assert float((g - rf).abs().max()) <= 1e-3 * rms  # FP32 sums in another order
+    assert torch.equal(bits(C.to(torch.bfloat16)), bits(lib.moe_gemm(x.to(DEV), 4, W, r)))
+
+
 # ---- top-k sum and the whole layer --------------------------------------------------------------
 
 def test_topk_sum_parity(lib):
     rng = np.random.default_rng(8)
     T, k, H = 33, 8, 2048
-    Y = torch.from_numpy(rng.standard_normal((T * k, H)).astype(np.float32)).to(torch.bfloat16)
+    Y = torch.from_numpy(rng.standard_normal((T * k, H)).astype(np.float32) * 10)
     ids = torch.from_numpy(rng.integers(-1, 5, (T, k)).astype(np.int32))
     w = torch.from_numpy(rng.random((T, k)).astype(np.float32))
     out = lib.topk_sum(Y.to(DEV), ids.to(DEV), w.to(DEV))

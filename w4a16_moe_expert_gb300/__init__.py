@@ -25,13 +25,14 @@ __all__ = [
     "load", "library_path", "align_capacity", "moe_align", "PackedWeights", "pack_weights",
     "Routing", "moe_gemm", "topk_sum", "moe_layer", "layer_workspace_size", "plan_block_m",
     "plan_gemm", "debug_dequant", "gemm_workspace_size", "EPILOGUE_NONE", "EPILOGUE_SILU_MUL",
-    "A_ROWS_SORTED", "C_ROWS_SORTED", "PACK_GATE_UP_PAIRED", "LibraryError",
+    "A_ROWS_SORTED", "C_ROWS_SORTED", "C_FP32", "PACK_GATE_UP_PAIRED", "LibraryError",
 ]
 
 EPILOGUE_NONE = 0
 EPILOGUE_SILU_MUL = 1
 A_ROWS_SORTED = 0x1
 C_ROWS_SORTED = 0x2
+C_FP32 = 0x4
 PACK_GATE_UP_PAIRED = 0x1
 PACK_MAGIC = 0x3631413457454F4D
 PACK_VERSION = 1
@@ -268,8 +269,9 @@ def moe_gemm(A: torch.Tensor, a_row_div: int, W: PackedWeights, routing: Routing
     if out is None:
         rows = out_rows if out_rows is not None else (
             routing.capacity if row_flags & C_ROWS_SORTED else routing.total_slots)
-        out = torch.zeros((rows, width), dtype=torch.bfloat16, device=A.device)
-    _cuda(out, torch.bfloat16, "out")
+        out = torch.zeros((rows, width), dtype=torch.float32 if row_flags & C_FP32 else torch.bfloat16,
+                          device=A.device)
+    _cuda(out, torch.float32 if row_flags & C_FP32 else torch.bfloat16, "out")
     if workspace is None:
         workspace = gemm_workspace(routing.total_slots, W.E, W.N, W.K, routing.block_m, A.device)
     sched = ScheduleDesc(split_k, num_ctas)
@@ -283,7 +285,7 @@ def moe_gemm(A: torch.Tensor, a_row_div: int, W: PackedWeights, routing: Routing
 
 def topk_sum(Y: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
              out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    _cuda(Y, torch.bfloat16, "Y")
+    _cuda(Y, torch.float32, "Y")
     _cuda(topk_ids, torch.int32, "topk_ids")
     _cuda(topk_weights, torch.float32, "topk_weights")
     T, k = topk_ids.shape

@@ -92,7 +92,7 @@ static w4a16_status_t check_packed(const w4a16_packed_weights_t* W) {
 // ---- top-k weighted sum ---------------------------------------------------------------------------
 // One thread per 8 output columns of one token; FP32 accumulation over slots in order.
 __global__ void __launch_bounds__(256)
-    topk_sum_kernel(const uint16_t* __restrict__ Y, const int32_t* __restrict__ topk_ids,
+    topk_sum_kernel(const float* __restrict__ Y, const int32_t* __restrict__ topk_ids,
                     const float* __restrict__ topk_weights, int T, int top_k, int H,
                     uint16_t* __restrict__ out) {
   pdl_wait();  // Y is the previous kernel's output
@@ -106,13 +106,16 @@ __global__ void __launch_bounds__(256)
     const int64_t i = t * top_k + s;
     if (__ldg(topk_ids + i) < 0) continue;
     const float w = __ldg(topk_weights + i);
-    const uint4 y = __ldg(reinterpret_cast<const uint4*>(Y + i * H + c));
-    const uint32_t yw[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      acc[2 * q] += w * __uint_as_float(yw[q] << 16);
-      acc[2 * q + 1] += w * __uint_as_float(yw[q] & 0xffff0000u);
-    }
+    const float4 y0 = __ldg(reinterpret_cast<const float4*>(Y + i * H + c));
+    const float4 y1 = __ldg(reinterpret_cast<const float4*>(Y + i * H + c + 4));
+    acc[0] += w * y0.x;
+    acc[1] += w * y0.y;
+    acc[2] += w * y0.z;
+    acc[3] += w * y0.w;
+    acc[4] += w * y1.x;
+    acc[5] += w * y1.y;
+    acc[6] += w * y1.z;
+    acc[7] += w * y1.w;
   }
   uint32_t o[4];
 #pragma unroll
@@ -124,7 +127,7 @@ __global__ void __launch_bounds__(256)
   *reinterpret_cast<uint4*>(out + t * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-static cudaError_t launch_topk_sum(const uint16_t* Y, const int32_t* ids, const float* w, int T,
+static cudaError_t launch_topk_sum(const float* Y, const int32_t* ids, const float* w, int T,
                                    int top_k, int H, uint16_t* out, cudaStream_t stream) {
   const int64_t n = static_cast<int64_t>(T) * (H / 8);
   if (n == 0) return cudaSuccess;
@@ -182,6 +185,8 @@ static w4a16_status_t run_gemm(const GemmCall& c, const DeviceFacts& dev, cudaSt
     return fail(W4A16_INVALID_ARG, "unknown epilogue %d", c.epilogue);
   }
   if (c.ldc < out_cols) return fail(W4A16_INVALID_ARG, "ldc smaller than the output width");
+  if ((c.row_flags & W4A16_C_FP32) && c.epilogue != W4A16_EPILOGUE_NONE)
+    return fail(W4A16_INVALID_ARG, "FP32 output is available with epilogue NONE only");
   if (R->capacity == 0 || c.W->E == 0) return W4A16_OK;
 
   w4a16_plan_t plan;
@@ -218,6 +223,7 @@ static w4a16_status_t run_gemm(const GemmCall& c, const DeviceFacts& dev, cudaSt
   a.capacity = R->capacity;
   a.epilogue = c.epilogue;
   a.c_sorted = (c.row_flags & W4A16_C_ROWS_SORTED) ? 1 : 0;
+  a.c_f32 = (c.row_flags & W4A16_C_FP32) ? 1 : 0;
   a.C = c.C;
   a.ldc = c.ldc;
   a.cnt = static_cast<int32_t*>(c.ws);
@@ -350,14 +356,14 @@ w4a16_status_t w4a16_moe_gemm(const uint16_t* A, int64_t lda, int a_row_div,
   DeviceFacts dev;
   w4a16_status_t st = device_facts(&dev);
   if (st != W4A16_OK) return st;
-  if (row_flags & ~(W4A16_A_ROWS_SORTED | W4A16_C_ROWS_SORTED))
+  if (row_flags & ~(W4A16_A_ROWS_SORTED | W4A16_C_ROWS_SORTED | W4A16_C_FP32))
     return fail(W4A16_INVALID_ARG, "unknown row flags");
   GemmCall c{A, lda, a_row_div, W, routing, epilogue, row_flags, C, ldc, workspace,
              workspace_bytes, expected_rows_per_expert, schedule, dev_err, 0};
   return run_gemm(c, dev, stream);
 }
 
-w4a16_status_t w4a16_topk_sum(const uint16_t* Y, const int32_t* topk_ids,
+w4a16_status_t w4a16_topk_sum(const float* Y, const int32_t* topk_ids,
                               const float* topk_weights, int T, int top_k, int H,
                               uint16_t* out, w4a16_stream_t stream) {
   if (T < 0 || top_k <= 0 || H <= 0 || H % 8) return fail(W4A16_INVALID_ARG, "need H %% 8 == 0");
@@ -395,7 +401,7 @@ w4a16_status_t w4a16_plan_gemm(int total_slots, int E, int N, int K, int block_m
 
 // Layer workspace, in order (each piece 256-byte aligned):
 //   sorted_ids [cap] | expert_ids [cap / bm] | ntp [1] | K-split counters | K-split partials |
-//   h (SiLU output, sorted rows) [cap, I] BF16 | Y (down output, slot rows) [T*top_k, H] BF16
+//   h (SiLU output, sorted rows) [cap, I] BF16 | Y (down output, slot rows) [T*top_k, H] FP32
 struct LayerLayout {
   int block_m;
   int64_t cap;
@@ -420,7 +426,7 @@ static LayerLayout layer_layout(int T, int top_k, int E, int E_global, int H, in
   L.off_h = o;
   o = round_up(o + static_cast<size_t>(L.cap) * I * 2, 256);
   L.off_y = o;
-  o = round_up(o + static_cast<size_t>(T) * top_k * H * 2, 256);
+  o = round_up(o + static_cast<size_t>(T) * top_k * H * 4, 256);
   L.total = o;
   return L;
 }
@@ -465,7 +471,7 @@ w4a16_status_t w4a16_moe_layer(const uint16_t* x, const w4a16_packed_weights_t* 
   int32_t* expert_ids = reinterpret_cast<int32_t*>(ws + L.off_expert);
   int32_t* ntp = reinterpret_cast<int32_t*>(ws + L.off_ntp);
   uint16_t* h = reinterpret_cast<uint16_t*>(ws + L.off_h);
-  uint16_t* y = reinterpret_cast<uint16_t*>(ws + L.off_y);
+  float* y = reinterpret_cast<float*>(ws + L.off_y);
   const int n_slots = T * top_k;
 
   cudaError_t err = launch_moe_align(topk_ids, n_slots, E, L.block_m, sorted_ids, expert_ids, ntp,
@@ -480,7 +486,8 @@ w4a16_status_t w4a16_moe_layer(const uint16_t* x, const w4a16_packed_weights_t* 
   GemmCall g1{x, H, top_k, w13, &R, W4A16_EPILOGUE_SILU_MUL, W4A16_C_ROWS_SORTED, h, I,
               ws + L.off_cnt, (L.off_h - L.off_cnt), rows_hint, nullptr, dev_err, 0};
   if ((st = run_gemm(g1, dev, stream)) != W4A16_OK) return st;
-  GemmCall g2{h, I, 1, w2, &R, W4A16_EPILOGUE_NONE, W4A16_A_ROWS_SORTED, y, H,
+  GemmCall g2{h, I, 1, w2, &R, W4A16_EPILOGUE_NONE, W4A16_A_ROWS_SORTED | W4A16_C_FP32,
+              reinterpret_cast<uint16_t*>(y), H,
               ws + L.off_cnt, (L.off_h - L.off_cnt), rows_hint, nullptr, dev_err, 1};
   if ((st = run_gemm(g2, dev, stream)) != W4A16_OK) return st;
   err = launch_topk_sum(y, topk_ids, topk_weights, T, top_k, H, out, stream);

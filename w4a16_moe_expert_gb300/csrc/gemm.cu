@@ -116,7 +116,10 @@ __device__ __forceinline__ void store_column(const GemmArgs& a, const Unit& un, 
     a.C[row * a.ldc + col] = __bfloat16_as_ushort(__float2bfloat16_rn(h));
   } else {
     const int n = tile_row_to_canonical(un.jt, t, a.N, a.paired != 0);
-    a.C[row * a.ldc + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    if (a.c_f32)
+      reinterpret_cast<float*>(a.C)[row * a.ldc + n] = v;
+    else
+      a.C[row * a.ldc + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
   }
 }
 

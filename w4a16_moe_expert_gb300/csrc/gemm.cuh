@@ -21,6 +21,7 @@ struct GemmArgs {
   int64_t capacity;
   int epilogue;
   int c_sorted;
+  int c_f32;  // C is float (unrounded sums)
   uint16_t* C;
   int64_t ldc;
   float* part;
