@@ -148,7 +148,7 @@ w4a16_status_t w4a16_pack_weights(const int32_t* qweight, const uint16_t* scales
 #define W4A16_C_FP32 0x4u
 
 typedef struct {
-  const int32_t* sorted_ids;        /* device [capacity] */
+  const int32_t* sorted_ids;        /* device [capacity], 16-byte aligned */
   const int32_t* expert_ids;        /* device [capacity / block_m] */
   const int32_t* num_tokens_padded; /* device [1] */
   int64_t capacity;

@@ -168,6 +168,8 @@ static w4a16_status_t run_gemm(const GemmCall& c, const DeviceFacts& dev, cudaSt
   const w4a16_routing_t* R = c.R;
   if (!R || !R->sorted_ids || !R->expert_ids || !R->num_tokens_padded)
     return fail(W4A16_INVALID_ARG, "routing tensors must not be NULL");
+  if (reinterpret_cast<uintptr_t>(R->sorted_ids) % 16)
+    return fail(W4A16_INVALID_ARG, "sorted_ids must be 16-byte aligned");
   if (!valid_block_m(R->block_m))
     return fail(W4A16_UNSUPPORTED, "block_m %d: supported values are 16, 32, 64, 128", R->block_m);
   if (R->capacity < 0 || R->capacity % R->block_m || R->total_slots < 0)
@@ -203,7 +205,8 @@ static w4a16_status_t run_gemm(const GemmCall& c, const DeviceFacts& dev, cudaSt
   if (split > 1 && (!c.ws || c.ws_bytes < cnt_bytes + kPartialBytes))
     return fail(W4A16_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes", cnt_bytes + kPartialBytes);
 
-  GemmArgs a{};
+  GemmArgs a;
+  std::memset(&a, 0, sizeof a);
   a.A = c.A;
   a.lda = c.lda;
   a.a_row_div = c.a_row_div;

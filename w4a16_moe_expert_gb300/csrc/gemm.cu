@@ -14,11 +14,15 @@
 //   * the weight tile (128 rows of W[e] = MMA M) is the A operand, read from TMEM; tokens of
 //     one aligned block (block_m = MMA N) are the B operand, in 128-byte-swizzled shared
 //     memory; the FP32 accumulator is in TMEM;
-//   * warp 0 streams 4608-byte packed chunks with 1-D bulk TMA (evict_first for streamed
-//     weights); warps 2-3 gather activation rows with cp.async (row = sorted_ids[p] / div);
-//     warps 8-15 (two dequant warpgroups, alternating stages) turn codes into BF16 pairs and
-//     store them to TMEM with tcgen05.st; warp 1 issues tcgen05.mma from one thread; warps
-//     4-7 drain the double-buffered accumulator with tcgen05.ld and write BF16 results;
+//   * warp 0 streams the packed weights, one 1-D bulk copy per stage of one or two 64-wide K
+//     blocks (evict_first when weights are streamed once), and, when the activation rows are
+//     already in sorted order, their 2-D tiles by tensor TMA; otherwise warps 2-3 gather the
+//     rows (row = sorted_ids[p] / a_row_div) with 16-byte cp.async into the swizzled layout.
+//     Weights and activations complete on separate mbarriers, so a dependent launch streams
+//     and dequantises its first weights before its inputs exist;
+//   * warps 8-15 (two dequant warpgroups, alternating stages) turn codes into BF16 pairs and
+//     store them to TMEM with tcgen05.st; warp 1 issues tcgen05.mma from one elected lane;
+//     warps 4-7 drain the double-buffered accumulator with tcgen05.ld and write the results;
 //   * a persistent grid walks (block, 128-row tile, K split) units found from
 //     num_tokens_padded on the device (no host read-back); K splits (decode) write FP32
 //     partials and the last CTA to arrive on a per-tile counter sums them in split order,
@@ -32,24 +36,29 @@ namespace w4a16 {
 
 constexpr int kGemmThreads = 512;
 constexpr int kTmemCols = 512;
-constexpr int kACol0 = 256;  // TMEM columns [256, 512): dequantised A stages, 32 columns each
-constexpr int kAStages = 8;
-constexpr int kGatherThreads = 64;  // warps 2 and 3
+constexpr int kACol0 = 256;  // TMEM columns [256, 512): dequantised A stages
 constexpr int kSmemBudget = 200 * 1024;
+constexpr int kGatherThreads = 64;  // warps 2 and 3 gather activation rows with cp.async
 
-template <int NT>
+// NT = block_m = MMA N; KS = 64-wide K sub-blocks per pipeline stage (deeper stages halve the
+// per-byte barrier, copy-issue and commit overhead of the weight-bound decode shapes).
+template <int NT, int KS>
 struct GemmCfg {
-  static constexpr int kBBytes = NT * 128;  // NT rows x 64 BF16
-  static constexpr int kStageBytes = kBBytes + kChunkBytes;
-  static constexpr int kStagesRaw = (kSmemBudget - 2048) / kStageBytes;
+  static constexpr int kSubB = NT * 128;            // B bytes of one sub-block (NT rows x 64)
+  static constexpr int kBBytes = KS * kSubB;
+  static constexpr int kWBytes = KS * kChunkBytes;
+  static constexpr int kStageBytes = kBBytes + kWBytes;
+  static constexpr int kStagesRaw = (kSmemBudget - 4096) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 32 ? 32 : kStagesRaw;
+  static constexpr int kAStages = 8 / KS;           // each KS * 32 TMEM columns
   static constexpr int kBarBytes = (3 * kStages + 2 * kAStages + 5) * 8;
-  static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + kBarBytes + 64;
+  static constexpr size_t kSmemBytes =
+      1024 + static_cast<size_t>(kStages) * kStageBytes + kBarBytes + 64 + NT * 4;
   static_assert(NT % 16 == 0 && NT >= 16 && NT <= 128, "MMA N must be 16..128 in steps of 16");
   static_assert(2 * NT <= kACol0, "accumulators must fit below the A stages");
+  static_assert(kACol0 + 32 * KS * kAStages <= kTmemCols, "A stages must fit in TMEM");
+  static_assert(kStages >= 4, "pipeline too shallow");
 };
-
-
 
 struct Unit {
   int b, jt, split, kb0, kb1, e;
@@ -93,52 +102,55 @@ __device__ __forceinline__ float bf16_round(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
 }
 
-// Store one accumulator column (token column j of the block) for tile row t.
+// Store one accumulator column (token column j of the block) for tile row t; `slot` is
+// sorted_ids at that position.
 __device__ __forceinline__ void store_column(const GemmArgs& a, const Unit& un, int t, int j,
-                                             float v) {
+                                             int32_t slot, float v) {
   // SiLU-and-mul needs the up value from lane + 16 of the same warp (all lanes shuffle).
   const float up = __shfl_down_sync(0xffffffffu, v, 16);
-  const int64_t p = static_cast<int64_t>(un.b) * a.block_m + j;
+  const bool routed = (slot >= 0 && slot < a.total_slots);
   int64_t row;
   if (a.c_sorted) {
-    row = p;
+    row = static_cast<int64_t>(un.b) * a.block_m + j;  // padding rows are written too, as zeros
   } else {
-    const int32_t i = __ldg(a.sorted_ids + p);
-    if (i >= a.total_slots || i < 0) return;
-    row = i;
+    if (!routed) return;
+    row = slot;
   }
   if (a.epilogue == W4A16_EPILOGUE_SILU_MUL) {
     const int l = t & 31;
     if (l >= 16) return;
     const float g = bf16_round(v), u = bf16_round(up);
-    const float h = g / (1.0f + expf(-g)) * u;
+    const float h = routed ? __fdividef(g, 1.0f + __expf(-g)) * u : 0.0f;
     const int col = 64 * un.jt + 16 * (t >> 5) + l;
     a.C[row * a.ldc + col] = __bfloat16_as_ushort(__float2bfloat16_rn(h));
   } else {
     const int n = tile_row_to_canonical(un.jt, t, a.N, a.paired != 0);
+    const float val = routed ? v : 0.0f;
     if (a.c_f32)
-      reinterpret_cast<float*>(a.C)[row * a.ldc + n] = v;
+      reinterpret_cast<float*>(a.C)[row * a.ldc + n] = val;
     else
-      a.C[row * a.ldc + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+      a.C[row * a.ldc + n] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
   }
 }
 
-template <int NT>
-__global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmArgs a) {
-  using Cfg = GemmCfg<NT>;
+template <int NT, int KS>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ GemmArgs a) {
+  using Cfg = GemmCfg<NT, KS>;
   constexpr int S_C = Cfg::kStages;
+  constexpr int S_A = Cfg::kAStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* base = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  uint8_t* b_ring = base;
-  uint8_t* c_ring = base + S_C * Cfg::kBBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(c_ring + S_C * kChunkBytes);
-  uint64_t* wfull = bars;
-  uint64_t* bfull = bars + S_C;
-  uint64_t* empty = bars + 2 * S_C;
-  uint64_t* afull = bars + 3 * S_C;
-  uint64_t* aempty = afull + kAStages;
-  uint64_t* accfull = aempty + kAStages;
+  uint8_t* b_ring = base;                                // S_C x KS x [NT rows x 128 B]
+  uint8_t* c_ring = base + S_C * Cfg::kBBytes;           // S_C x KS x 4608-byte chunks
+  uint64_t* bars = reinterpret_cast<uint64_t*>(c_ring + S_C * Cfg::kWBytes);
+  uint64_t* wfull = bars;             // packed weights of stage s landed
+  uint64_t* bfull = bars + S_C;       // activation rows of stage s landed
+  uint64_t* empty = bars + 2 * S_C;   // the MMAs reading stage s finished
+  uint64_t* afull = bars + 3 * S_C;   // dequantised A stage in TMEM written
+  uint64_t* aempty = afull + S_A;     // the MMAs reading A stage finished
+  uint64_t* accfull = aempty + S_A;
   uint64_t* accempty = accfull + 2;
   uint64_t* drain = accempty + 2;
   uint32_t* misc = reinterpret_cast<uint32_t*>(drain + 1);
@@ -146,16 +158,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(misc + 2);
   uint32_t* issued = misc + 3;
+  int32_t* epi_rows = reinterpret_cast<int32_t*>(misc + 16);  // sorted_ids of the unit's block
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool gather = !a.a_sorted;
 
   if (tid == 0) {
     for (int s = 0; s < S_C; ++s) {
       mbar_init(smem_u32(&wfull[s]), 1);
-      mbar_init(smem_u32(&bfull[s]), kGatherThreads);
+      mbar_init(smem_u32(&bfull[s]), gather ? kGatherThreads : 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
-    for (int s = 0; s < kAStages; ++s) {
+    for (int s = 0; s < S_A; ++s) {
       mbar_init(smem_u32(&afull[s]), 128);
       mbar_init(smem_u32(&aempty[s]), 1);
     }
@@ -169,6 +183,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     *issued = 0;
     fence_mbar_init();
   }
+  if (warp == 0 && lane == 0 && !gather) tma_prefetch_desc(&a.tmap_a);
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -193,99 +208,153 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   const int64_t n_units = nblocks * a.n_tiles * split_k;
 
   if (warp == 0) {
-    // ---------------- weight stream: one bulk TMA per stage ----------------
-    if (lane == 0) {
-      const uint64_t policy = a.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
-      uint32_t it = 0;
-      for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
+    // ---------------- producer: weight chunks (bulk TMA), sorted activation tiles (TMA) -------
+    const uint64_t policy = a.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
+    auto chunk_src = [&](const Unit& un, int kb) {
+      return a.wblob + kHeaderBytes +
+             ((static_cast<int64_t>(un.e) * a.n_tiles + un.jt) * a.n_kb + kb) * kChunkBytes;
+    };
+    // Weights never depend on the previous kernel: with routing already complete, stream the
+    // first S_C stages before waiting for the activations (programmatic dependent launch).
+    uint32_t pre = 0;
+    if (a.routing_ready) {
+      for (int64_t u = blockIdx.x; u < n_units && pre < static_cast<uint32_t>(S_C); u += gridDim.x) {
         const Unit un = decode_unit(a, split_k, u);
         if (!un.ok) continue;
-        const uint8_t* src = a.wblob + kHeaderBytes +
-                             ((static_cast<int64_t>(un.e) * a.n_tiles + un.jt) * a.n_kb) * kChunkBytes;
-        for (int kb = un.kb0; kb < un.kb1; ++kb, ++it) {
-          const int s = it % S_C;
-          const uint32_t ph = (it / S_C) & 1;
-          if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, abort_flag, a.dev_err)) goto weights_done;
-          mbar_arrive_expect_tx(smem_u32(&wfull[s]), kChunkBytes);
-          bulk_g2s(smem_u32(c_ring + s * kChunkBytes), src + static_cast<int64_t>(kb) * kChunkBytes,
-                   kChunkBytes, smem_u32(&wfull[s]), policy);
+        for (int kb = un.kb0; kb < un.kb1 && pre < static_cast<uint32_t>(S_C); kb += KS, ++pre) {
+          const int nsub = min(KS, un.kb1 - kb);
+          if (lane == 0) {
+            const uint32_t wb = smem_u32(&wfull[pre]);
+            mbar_arrive_expect_tx(wb, nsub * kChunkBytes);
+            bulk_g2s(smem_u32(c_ring + pre * Cfg::kWBytes), chunk_src(un, kb), nsub * kChunkBytes,
+                     wb, policy);
+          }
         }
       }
-    weights_done:
-      *issued = it;
+      __syncwarp();
     }
-  } else if (warp == 2 || warp == 3) {
-    // ---------------- activation gather: cp.async rows into swizzled tiles ----------------
     pdl_wait();  // activations may be the previous kernel's output
-    const int g = tid - 64;
     uint32_t it = 0;
     for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
       const Unit un = decode_unit(a, split_k, u);
       if (!un.ok) continue;
-      for (int kb = un.kb0; kb < un.kb1; ++kb, ++it) {
+      for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
+        const int nsub = min(KS, un.kb1 - kb);
         const int s = it % S_C;
         const uint32_t ph = (it / S_C) & 1;
-        if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, abort_flag, a.dev_err)) goto gather_done;
-        const uint32_t bdst = smem_u32(b_ring + s * Cfg::kBBytes);
-        for (int idx = g; idx < NT * 8; idx += kGatherThreads) {
-          const int r = idx >> 3, c = idx & 7;
-          const int64_t p = static_cast<int64_t>(un.b) * a.block_m + r;
-          int64_t arow;
-          bool valid = true;
-          if (a.a_sorted) {
-            arow = p;
-          } else {
-            const int32_t i = __ldg(a.sorted_ids + p);
-            valid = (i >= 0 && i < a.total_slots);
-            arow = valid ? i / a.a_row_div : 0;
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[s]), ph ^ 1, abort_flag, a.dev_err)))
+          goto producer_done;
+        if (lane == 0) {
+          if (it >= pre) {
+            const uint32_t wb = smem_u32(&wfull[s]);
+            mbar_arrive_expect_tx(wb, nsub * kChunkBytes);
+            bulk_g2s(smem_u32(c_ring + s * Cfg::kWBytes), chunk_src(un, kb), nsub * kChunkBytes,
+                     wb, policy);
           }
-          const uint16_t* src = a.A + arow * a.lda + kb * kBlockK + c * 8;
-          cp_async_16(bdst + r * 128 + ((c ^ (r & 7)) << 4), valid ? src : a.A, valid ? 16u : 0u);
+          if (!gather) {
+            const uint32_t bb = smem_u32(&bfull[s]);
+            mbar_arrive_expect_tx(bb, nsub * Cfg::kSubB);
+            for (int sb = 0; sb < nsub; ++sb)
+              tma_load_2d(smem_u32(b_ring + s * Cfg::kBBytes + sb * Cfg::kSubB), &a.tmap_a,
+                          (kb + sb) * kBlockK, static_cast<int>(un.b * a.block_m), bb);
+          }
         }
-        cp_async_arrive_noinc(smem_u32(&bfull[s]));
+        __syncwarp();
       }
     }
-  gather_done:
-    cp_async_wait_all();
-  } else if (warp == 1) {
-    // ---------------- MMA issue (one thread) ----------------
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, NT);
-      uint32_t it = 0, lu = 0;
+  producer_done:
+    if (lane == 0) *issued = it > pre ? it : pre;
+  } else if (warp == 2 || warp == 3) {
+    // ---------------- activation row gather (cp.async, 128-byte swizzled rows) ----------------
+    if (gather) {
+      pdl_wait();  // activations may be the previous kernel's output
+      const int g = tid - 64;
+      const int c = g & 7;  // 16-byte chunk of a 128-byte row handled by this thread
+      constexpr int R = NT / 8;  // rows per thread: (g >> 3) + 8j
+      uint32_t it = 0;
       for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
         const Unit un = decode_unit(a, split_k, u);
         if (!un.ok) continue;
-        const int ab = lu & 1;
-        const uint32_t pab = (lu >> 1) & 1;
-        if (!mbar_wait(smem_u32(&accempty[ab]), pab ^ 1, abort_flag, a.dev_err)) goto mma_done;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + ab * NT;
-        for (int kb = un.kb0; kb < un.kb1; ++kb, ++it) {
+        int32_t arow[R];
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          const int32_t i = __ldg(a.sorted_ids + static_cast<int64_t>(un.b) * a.block_m + (g >> 3) + 8 * j);
+          arow[j] = (i >= 0 && i < a.total_slots) ? i / a.a_row_div : -1;
+        }
+        for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
+          const int nsub = min(KS, un.kb1 - kb);
           const int s = it % S_C;
           const uint32_t ph = (it / S_C) & 1;
-          const int sa = it % kAStages;
-          const uint32_t pa = (it / kAStages) & 1;
-          if (!mbar_wait(smem_u32(&bfull[s]), ph, abort_flag, a.dev_err)) goto mma_done;
-          if (!mbar_wait(smem_u32(&afull[sa]), pa, abort_flag, a.dev_err)) goto mma_done;
-          fence_proxy_async_smem();  // cp.async (generic proxy) data -> tensor core reads
-          tc_fence_after();
-          const uint32_t b_addr = smem_u32(b_ring + s * Cfg::kBBytes);
-          const uint32_t a_tmem = tmem_base + kACol0 + sa * 32;
+          if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, abort_flag, a.dev_err)) goto gather_done;
+          const uint32_t bdst = smem_u32(b_ring + s * Cfg::kBBytes);
+          for (int sb = 0; sb < nsub; ++sb) {
 #pragma unroll
-          for (int kk = 0; kk < kBlockK / 16; ++kk) {
-            mma_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(b_addr + kk * 32), idesc,
-                   (kb > un.kb0 || kk > 0) ? 1u : 0u);
+            for (int j = 0; j < R; ++j) {
+              const int r = (g >> 3) + 8 * j;
+              const uint32_t dst = bdst + sb * Cfg::kSubB + r * 128 + ((c ^ (r & 7)) << 4);
+              const uint16_t* src = arow[j] >= 0
+                                        ? a.A + static_cast<int64_t>(arow[j]) * a.lda + (kb + sb) * kBlockK + c * 8
+                                        : a.A;
+              cp_async_16(dst, src, arow[j] >= 0 ? 16u : 0u);
+            }
+          }
+          cp_async_arrive_noinc(smem_u32(&bfull[s]));
+        }
+      }
+    gather_done:
+      cp_async_wait_all();
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issue: warp-wide loop, one elected lane issues ----------------
+    constexpr uint32_t idesc = idesc_bf16_f32(128, NT);
+    const uint64_t b_desc0 = smem_desc_sw128(smem_u32(b_ring));
+    uint32_t it = 0, lu = 0;
+    for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
+      const Unit un = decode_unit(a, split_k, u);
+      if (!un.ok) continue;
+      const int ab = lu & 1;
+      const uint32_t pab = (lu >> 1) & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&accempty[ab]), pab ^ 1, abort_flag, a.dev_err)))
+        goto mma_done;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + ab * NT;
+      for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
+        const int nsub = min(KS, un.kb1 - kb);
+        const int s = it % S_C;
+        const uint32_t ph = (it / S_C) & 1;
+        const int sa = it % S_A;
+        const uint32_t pa = (it / S_A) & 1;
+        bool ok = mbar_wait(smem_u32(&bfull[s]), ph, abort_flag, a.dev_err);
+        ok = ok && mbar_wait(smem_u32(&afull[sa]), pa, abort_flag, a.dev_err);
+        if (!__all_sync(0xffffffffu, ok)) goto mma_done;
+        if (gather) fence_proxy_async_smem();  // cp.async (generic proxy) rows -> tensor core
+        tc_fence_after();
+        const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((s * Cfg::kBBytes) >> 4);
+        const uint32_t a_tmem = tmem_base + kACol0 + sa * (KS * 32);
+        if (elect_one()) {
+          for (int sb = 0; sb < nsub; ++sb) {
+            const uint64_t bd = b_desc + static_cast<uint64_t>((sb * Cfg::kSubB) >> 4);
+            const uint32_t at = a_tmem + sb * 32;
+            mma_ts(d_tmem, at, bd, idesc, (kb > un.kb0 || sb > 0) ? 1u : 0u);
+            mma_ts(d_tmem, at + 8, bd + 2, idesc, 1u);
+            mma_ts(d_tmem, at + 16, bd + 4, idesc, 1u);
+            mma_ts(d_tmem, at + 24, bd + 6, idesc, 1u);
           }
           mma_commit(smem_u32(&empty[s]));
           mma_commit(smem_u32(&aempty[sa]));
         }
-        mma_commit(smem_u32(&accfull[ab]));
-        ++lu;
+        __syncwarp();
       }
-    mma_done:
+      if (elect_one()) mma_commit(smem_u32(&accfull[ab]));
+      __syncwarp();
+      ++lu;
+    }
+  mma_done:
+    if (elect_one()) {
       mma_commit(smem_u32(drain));
       mbar_wait_plain(smem_u32(drain), 0);
     }
+    __syncwarp();
   } else if (warp >= 4 && warp < 8) {
     // ---------------- epilogue warpgroup ----------------
     pdl_wait();  // outputs may still be read by the previous kernel
@@ -295,6 +364,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
       const Unit un = decode_unit(a, split_k, u);
       if (!un.ok) continue;
+      named_bar_epi();  // the previous unit's readers of epi_rows are done
+      if (t < NT) epi_rows[t] = __ldg(a.sorted_ids + static_cast<int64_t>(un.b) * a.block_m + t);
+      named_bar_epi();
       const int ab = lu & 1;
       const uint32_t pab = (lu >> 1) & 1;
       const bool ok = mbar_wait(smem_u32(&accfull[ab]), pab, abort_flag, a.dev_err);
@@ -312,7 +384,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
             mbar_arrive(smem_u32(&accempty[ab]));
           }
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) store_column(a, un, t, c0 + jj, __uint_as_float(r[jj]));
+          for (int jj = 0; jj < 16; ++jj)
+            store_column(a, un, t, c0 + jj, epi_rows[c0 + jj], __uint_as_float(r[jj]));
         }
       } else {
         float* part = a.part + (un.tile * split_k + un.split) * (128 * NT);
@@ -339,11 +412,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
           for (int j = 0; j < NT; ++j) {
             float v = 0.0f;
             for (int s = 0; s < split_k; ++s) v += __ldcg(tile_parts + s * (128 * NT) + j * 128 + t);
-            store_column(a, un, t, j, v);
+            store_column(a, un, t, j, epi_rows[j], v);
           }
           if (t == 0) a.cnt[un.tile] = 0;  // ready for the next call
         }
-        named_bar_epi();
       }
       ++lu;
     }
@@ -357,25 +429,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
       const Unit un = decode_unit(a, split_k, u);
       if (!un.ok) continue;
-      for (int kb = un.kb0; kb < un.kb1; ++kb, ++it) {
+      for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
         if ((it & 1) != static_cast<uint32_t>(g)) continue;
+        const int nsub = min(KS, un.kb1 - kb);
         const int s = it % S_C;
         const uint32_t ph = (it / S_C) & 1;
-        const int sa = it % kAStages;
-        const uint32_t pa = (it / kAStages) & 1;
+        const int sa = it % S_A;
+        const uint32_t pa = (it / S_A) & 1;
         // warp-uniform decisions: tcgen05.st below is a warp-collective instruction
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&wfull[s]), ph, abort_flag, a.dev_err)))
           goto dq_done;
-        const uint8_t* ch = c_ring + s * kChunkBytes;
-        const uint4 lo = reinterpret_cast<const uint4*>(ch)[t];
-        const uint4 hi = reinterpret_cast<const uint4*>(ch + kCodeHalfBytes)[t];
-        const uint32_t s2 = reinterpret_cast<const uint32_t*>(ch + kScaleOffset)[t];
-        uint32_t v[32];
-        dequant_row64(lo, hi, s2, v);
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&aempty[sa]), pa ^ 1, abort_flag, a.dev_err)))
-          goto dq_done;
-        tc_fence_after();
-        tmem_st32(lane_base + sa * 32, v);
+        for (int sb = 0; sb < nsub; ++sb) {
+          const uint8_t* ch = c_ring + s * Cfg::kWBytes + sb * kChunkBytes;
+          const uint4 lo = reinterpret_cast<const uint4*>(ch)[t];
+          const uint4 hi = reinterpret_cast<const uint4*>(ch + kCodeHalfBytes)[t];
+          const uint32_t s2 = reinterpret_cast<const uint32_t*>(ch + kScaleOffset)[t];
+          uint32_t v[32];
+          dequant_row64(lo, hi, s2, v);
+          if (sb == 0) {
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(smem_u32(&aempty[sa]), pa ^ 1, abort_flag, a.dev_err)))
+              goto dq_done;
+            tc_fence_after();
+          }
+          tmem_st32(lane_base + sa * (KS * 32) + sb * 32, v);
+        }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(smem_u32(&afull[sa]));
@@ -386,10 +464,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
 
   __syncthreads();
   if (*abort_flag && warp == 0 && lane == 0) {
-    // give in-flight weight copies a bounded chance to land before the CTA's memory goes away
+    // give in-flight copies a bounded chance to land before the CTA's memory goes away
     const uint32_t n = *issued;
-    for (uint32_t j = (n > static_cast<uint32_t>(S_C) ? n - S_C : 0); j < n; ++j)
+    for (uint32_t j = (n > static_cast<uint32_t>(S_C) ? n - S_C : 0); j < n; ++j) {
       mbar_wait_plain(smem_u32(&wfull[j % S_C]), (j / S_C) & 1);
+      if (!gather) mbar_wait_plain(smem_u32(&bfull[j % S_C]), (j / S_C) & 1);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -400,15 +480,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
 }
 
 // ------------------------------------------------------------------------------------------
-// Host side: planner and launcher.
+// Host side: planner, tensor maps and launcher.
 // ------------------------------------------------------------------------------------------
+
+// Stage depth per block_m: two 64-wide K sub-blocks per stage for the weight-bound small
+// blocks, one for the larger blocks (shared memory then goes to activation tiles).
+template <int NT> struct StageK { static constexpr int value = NT <= 32 ? 2 : 1; };
 
 int stages_for_block_m(int block_m) {
   switch (block_m) {
-    case 16: return GemmCfg<16>::kStages;
-    case 32: return GemmCfg<32>::kStages;
-    case 64: return GemmCfg<64>::kStages;
-    case 128: return GemmCfg<128>::kStages;
+    case 16: return GemmCfg<16, StageK<16>::value>::kStages;
+    case 32: return GemmCfg<32, StageK<32>::value>::kStages;
+    case 64: return GemmCfg<64, StageK<64>::value>::kStages;
+    case 128: return GemmCfg<128, StageK<128>::value>::kStages;
     default: return 0;
   }
 }
@@ -450,12 +534,49 @@ void plan_gemm(int total_slots, int E, int N, int K, int block_m, int rows_per_e
   plan->stages = stages_for_block_m(block_m);
 }
 
+// cuTensorMapEncodeTiled from the driver (fetched once; no link-time libcuda dependency).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// Activations as a 2-D BF16 tensor [rows, K] with row stride lda, 128-byte swizzle; the box is
+// 64 columns by box_rows rows (1 for four-row gathers, block_m for sorted tiles).
+cudaError_t make_act_tmap(CUtensorMap* map, const uint16_t* A, int64_t rows, int K, int64_t lda,
+                          int box_rows) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(lda) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockK), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(A), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int NT>
-cudaError_t launch_gemm_t(const GemmArgs& args, int grid, bool pdl, cudaStream_t stream) {
-  using Cfg = GemmCfg<NT>;
+cudaError_t launch_gemm_t(GemmArgs& args, int grid, bool pdl, cudaStream_t stream) {
+  constexpr int KS = StageK<NT>::value;
+  using Cfg = GemmCfg<NT, KS>;
   static bool configured = false;  // per-process; attribute applies to the current device
   if (!configured) {
-    cudaError_t err = cudaFuncSetAttribute(moe_gemm_kernel<NT>,
+    cudaError_t err = cudaFuncSetAttribute(moe_gemm_kernel<NT, KS>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(Cfg::kSmemBytes));
     if (err != cudaSuccess) return err;
@@ -471,10 +592,19 @@ cudaError_t launch_gemm_t(const GemmArgs& args, int grid, bool pdl, cudaStream_t
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, moe_gemm_kernel<NT>, args);
+  return cudaLaunchKernelEx(&cfg, moe_gemm_kernel<NT, KS>, args);
 }
 
-cudaError_t launch_gemm(const GemmArgs& args, int grid, bool pdl, cudaStream_t stream) {
+cudaError_t launch_gemm(GemmArgs& args, int grid, bool pdl, cudaStream_t stream) {
+  const int64_t rows = args.a_sorted
+                           ? args.capacity
+                           : (static_cast<int64_t>(args.total_slots) + args.a_row_div - 1) /
+                                 args.a_row_div;
+  if (rows <= 0) return cudaSuccess;  // nothing can be routed
+  if (args.a_sorted) {  // sorted rows: one 2-D TMA tile of block_m rows per K sub-block
+    cudaError_t err = make_act_tmap(&args.tmap_a, args.A, rows, args.K, args.lda, args.block_m);
+    if (err != cudaSuccess) return err;
+  }
   switch (args.block_m) {
     case 16: return launch_gemm_t<16>(args, grid, pdl, stream);
     case 32: return launch_gemm_t<32>(args, grid, pdl, stream);

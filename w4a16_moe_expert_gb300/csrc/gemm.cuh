@@ -1,11 +1,14 @@
 // Arguments of the indexed GEMM kernel, shared by the launcher and the C ABI layer.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (types only; the encoder is fetched from the driver at run time)
+
 #include "common.cuh"
 
 namespace w4a16 {
 
 struct GemmArgs {
+  CUtensorMap tmap_a;  // activations: box 64 x 1 (row gather) or 64 x block_m (sorted rows)
   const uint16_t* A;
   int64_t lda;
   int a_row_div;
@@ -33,7 +36,7 @@ struct GemmArgs {
   int routing_ready;  // routing was complete before the previous kernel started
 };
 
-cudaError_t launch_gemm(const GemmArgs& args, int grid, bool pdl, cudaStream_t stream);
+cudaError_t launch_gemm(GemmArgs& args, int grid, bool pdl, cudaStream_t stream);
 void plan_gemm(int total_slots, int E, int N, int K, int block_m, int rows_per_expert,
                int num_sms, w4a16_plan_t* plan);
 
