@@ -21,6 +21,7 @@ of the same workload and reports the same metric.
 from __future__ import annotations
 
 import argparse
+import inspect
 import json
 import os
 import statistics
@@ -205,37 +206,50 @@ def run_ours(args, rank, world, local_rank):
             flush.zero_()
             path(c, events[i] if events else None)
 
-    # warm-up
-    for _ in range(args.warmup):
+    # Step events: with CUDA-graph capture (events recorded as graph nodes) the device times
+    # carry no host launch gaps; without support for that, the step runs eagerly.
+    use_graph = "external" in inspect.signature(torch.cuda.Event.__new__).parameters and not args.eager
+    mk = (lambda: torch.cuda.Event(enable_timing=True, external=True)) if use_graph else \
+         (lambda: torch.cuda.Event(enable_timing=True))
+    step_events = [[mk() for _ in range(5)] for _ in cases]
+
+    for _ in range(args.warmup):  # eager warm-up (sets kernel attributes before any capture)
         step()
     torch.cuda.synchronize()
+    graph = None
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step(step_events)
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
 
     # timed region: device time from events, barrier + synchronize on both sides
-    all_events = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in cases]
-                  for _ in range(args.steps)]
     sampler = ClockSampler(local_rank)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     sampler.start()
     time.sleep(0.3)
+    stage_acc = [np.zeros(4) for _ in cases]
     t0 = time.perf_counter()
     for s in range(args.steps):
-        step(all_events[s])
-    torch.cuda.synchronize()
+        if graph is not None:
+            graph.replay()
+        else:
+            step(step_events)
+        torch.cuda.synchronize()
+        for i in range(len(cases)):
+            ev = step_events[i]
+            stage_acc[i] += [ev[j].elapsed_time(ev[j + 1]) * 1e3 for j in range(4)]
     wall = time.perf_counter() - t0
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
 
     # per-T stage times (mean over steps, microseconds)
-    stage_us = []
-    for i, c in enumerate(cases):
-        acc = np.zeros(4)
-        for s in range(args.steps):
-            ev = all_events[s][i]
-            acc += [ev[j].elapsed_time(ev[j + 1]) * 1e3 for j in range(4)]
-        stage_us.append(acc / args.steps)
+    stage_us = [acc / args.steps for acc in stage_acc]
     step_ms = float(sum(u.sum() for u in stage_us)) / 1e3
 
     # e2e through the public layer call, host buffers, copies inside the timed region
@@ -313,6 +327,9 @@ def run_ours(args, rank, world, local_rank):
                         f"uint4 group-32 BF16 scales",
             "tokens": tokens,
             "l2": "flushed by a 512 MB memset before every T (outside the timed events)",
+            "timing": ("CUDA graph of the step replayed K times; CUDA events recorded as graph "
+                       "nodes around every kernel" if use_graph else
+                       "eager launches; CUDA events around every kernel"),
             "parallelism": "replicas" if world > 1 else "single GPU",
             "sweep": sweep,
         },
@@ -415,6 +432,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     ap.add_argument("--ref-step-budget", type=float, default=4.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="time eager launches instead of a graph")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps are required")

@@ -34,30 +34,44 @@
 
 namespace w4a16 {
 
-constexpr int kGemmThreads = 512;
+constexpr int kDqGroups = 2;  // dequant warpgroups; stage it goes to group it % kDqGroups
+constexpr int kGemmThreads = 256 + 128 * kDqGroups;
 constexpr int kTmemCols = 512;
-constexpr int kACol0 = 256;  // TMEM columns [256, 512): dequantised A stages
-constexpr int kSmemBudget = 200 * 1024;
+constexpr int kSmemBudget = 224 * 1024;
 constexpr int kGatherThreads = 64;  // warps 2 and 3 gather activation rows with cp.async
 
-// NT = block_m = MMA N; KS = 64-wide K sub-blocks per pipeline stage (deeper stages halve the
-// per-byte barrier, copy-issue and commit overhead of the weight-bound decode shapes).
+// NT = block_m = MMA N; KS = 64-wide K sub-blocks per pipeline stage (one weight copy of
+// KS * 4608 bytes; deeper stages halve the per-byte barrier, copy and commit overhead).
+// Three independent rings: packed weights in shared memory (freed once the dequant warps hold
+// them in registers), activation tiles in shared memory (freed by the MMA commit), dequantised
+// weights in TMEM (freed by the MMA commit).
 template <int NT, int KS>
 struct GemmCfg {
   static constexpr int kSubB = NT * 128;            // B bytes of one sub-block (NT rows x 64)
-  static constexpr int kBBytes = KS * kSubB;
-  static constexpr int kWBytes = KS * kChunkBytes;
-  static constexpr int kStageBytes = kBBytes + kWBytes;
-  static constexpr int kStagesRaw = (kSmemBudget - 4096) / kStageBytes;
-  static constexpr int kStages = kStagesRaw > 32 ? 32 : kStagesRaw;
-  static constexpr int kAStages = 8 / KS;           // each KS * 32 TMEM columns
-  static constexpr int kBarBytes = (3 * kStages + 2 * kAStages + 5) * 8;
-  static constexpr size_t kSmemBytes =
-      1024 + static_cast<size_t>(kStages) * kStageBytes + kBarBytes + 64 + NT * 4;
+  static constexpr int kBBytes = KS * kSubB;        // one activation stage
+  static constexpr int kWBytes = KS * kChunkBytes;  // one weight stage
+  // activation ring: 64-96 KB (at least 4, at most 24 stages), the rest for weights.  The
+  // rows arrive with multi-microsecond latency under full HBM load and each slot is held until
+  // its MMAs finish, so the ring must cover that round trip.
+  static constexpr int kBBudget = (NT <= 32 ? 64 : 96) * 1024;
+  static constexpr int kBStagesRaw = kBBudget / kBBytes;
+  static constexpr int kBStages = kBStagesRaw < 4 ? 4 : (kBStagesRaw > 24 ? 24 : kBStagesRaw);
+  static constexpr int kWStagesRaw = (kSmemBudget - 4096 - kBStages * kBBytes) / kWBytes;
+  static constexpr int kWStages = kWStagesRaw > 32 ? 32 : kWStagesRaw;
+  // TMEM: two FP32 accumulators of NT columns at [0, 2 NT), then as many dequantised A stages
+  // of KS * 32 columns as fit (a deep A ring covers the dequant -> MMA -> commit round trip).
+  static constexpr int kACol0 = (2 * NT + 31) / 32 * 32;
+  static constexpr int kAStagesRaw = (kTmemCols - kACol0) / (KS * 32);
+  static constexpr int kAStages = kAStagesRaw > 12 ? 12 : kAStagesRaw;
+  static constexpr int kBarBytes = (2 * kWStages + 2 * kBStages + 2 * kAStages + 5) * 8;
+  static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kBStages) * kBBytes +
+                                       static_cast<size_t>(kWStages) * kWBytes + kBarBytes + 64 +
+                                       NT * 4;
   static_assert(NT % 16 == 0 && NT >= 16 && NT <= 128, "MMA N must be 16..128 in steps of 16");
-  static_assert(2 * NT <= kACol0, "accumulators must fit below the A stages");
   static_assert(kACol0 + 32 * KS * kAStages <= kTmemCols, "A stages must fit in TMEM");
-  static_assert(kStages >= 4, "pipeline too shallow");
+  static_assert(kAStages >= 2, "A ring too shallow");
+  static_assert(kWStages >= 4, "weight ring too shallow");
+  static_assert(kSmemBytes <= 232448, "shared memory (227 KB per block)");
 };
 
 struct Unit {
@@ -103,11 +117,9 @@ __device__ __forceinline__ float bf16_round(float x) {
 }
 
 // Store one accumulator column (token column j of the block) for tile row t; `slot` is
-// sorted_ids at that position.
+// sorted_ids at that position.  Epilogue NONE only.
 __device__ __forceinline__ void store_column(const GemmArgs& a, const Unit& un, int t, int j,
                                              int32_t slot, float v) {
-  // SiLU-and-mul needs the up value from lane + 16 of the same warp (all lanes shuffle).
-  const float up = __shfl_down_sync(0xffffffffu, v, 16);
   const bool routed = (slot >= 0 && slot < a.total_slots);
   int64_t row;
   if (a.c_sorted) {
@@ -116,20 +128,53 @@ __device__ __forceinline__ void store_column(const GemmArgs& a, const Unit& un, 
     if (!routed) return;
     row = slot;
   }
-  if (a.epilogue == W4A16_EPILOGUE_SILU_MUL) {
-    const int l = t & 31;
-    if (l >= 16) return;
-    const float g = bf16_round(v), u = bf16_round(up);
-    const float h = routed ? __fdividef(g, 1.0f + __expf(-g)) * u : 0.0f;
-    const int col = 64 * un.jt + 16 * (t >> 5) + l;
-    a.C[row * a.ldc + col] = __bfloat16_as_ushort(__float2bfloat16_rn(h));
+  const int n = tile_row_to_canonical(un.jt, t, a.N, a.paired != 0);
+  const float val = routed ? v : 0.0f;
+  if (a.c_f32)
+    reinterpret_cast<float*>(a.C)[row * a.ldc + n] = val;
+  else
+    a.C[row * a.ldc + n] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+}
+
+// SiLU-and-mul for token columns j (even) and j + 1 of a paired gate/up tile.  Lane l < 16
+// holds gate rows and lane l + 16 the matching up rows; after one exchange lane l computes
+// column j and lane l + 16 column j + 1, so every lane does useful work.
+__device__ __forceinline__ void store_silu_pair(const GemmArgs& a, const Unit& un, int t, int j,
+                                                int32_t slot0, int32_t slot1, float v0, float v1) {
+  const int l = t & 31;
+  const bool hi = l >= 16;
+  // lanes < 16 send their column j+1 gate to lane + 16; lanes >= 16 send their column j up
+  const float send = hi ? v0 : v1;
+  const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+  const float g = bf16_round(hi ? recv : v0);
+  const float u = bf16_round(hi ? v1 : recv);
+  const int jj = hi ? j + 1 : j;
+  const int32_t slot = hi ? slot1 : slot0;
+  const bool routed = (slot >= 0 && slot < a.total_slots);
+  int64_t row;
+  if (a.c_sorted) {
+    row = static_cast<int64_t>(un.b) * a.block_m + jj;
   } else {
-    const int n = tile_row_to_canonical(un.jt, t, a.N, a.paired != 0);
-    const float val = routed ? v : 0.0f;
-    if (a.c_f32)
-      reinterpret_cast<float*>(a.C)[row * a.ldc + n] = val;
-    else
-      a.C[row * a.ldc + n] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+    if (!routed) return;
+    row = slot;
+  }
+  const float h = routed ? __fdividef(g, 1.0f + __expf(-g)) * u : 0.0f;
+  const int col = 64 * un.jt + 16 * (t >> 5) + (l & 15);
+  a.C[row * a.ldc + col] = __bfloat16_as_ushort(__float2bfloat16_rn(h));
+}
+
+// All NT columns of one accumulator chunk of 16 (registers r) starting at column c0.
+__device__ __forceinline__ void store_chunk16(const GemmArgs& a, const Unit& un, int t, int c0,
+                                              const int32_t* rows, const uint32_t (&r)[16]) {
+  if (a.epilogue == W4A16_EPILOGUE_SILU_MUL) {
+#pragma unroll
+    for (int jj = 0; jj < 16; jj += 2)
+      store_silu_pair(a, un, t, c0 + jj, rows[c0 + jj], rows[c0 + jj + 1], __uint_as_float(r[jj]),
+                      __uint_as_float(r[jj + 1]));
+  } else {
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj)
+      store_column(a, un, t, c0 + jj, rows[c0 + jj], __uint_as_float(r[jj]));
   }
 }
 
@@ -137,19 +182,21 @@ template <int NT, int KS>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmArgs a) {
   using Cfg = GemmCfg<NT, KS>;
-  constexpr int S_C = Cfg::kStages;
+  constexpr int S_W = Cfg::kWStages;
+  constexpr int S_B = Cfg::kBStages;
   constexpr int S_A = Cfg::kAStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* base = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  uint8_t* b_ring = base;                                // S_C x KS x [NT rows x 128 B]
-  uint8_t* c_ring = base + S_C * Cfg::kBBytes;           // S_C x KS x 4608-byte chunks
-  uint64_t* bars = reinterpret_cast<uint64_t*>(c_ring + S_C * Cfg::kWBytes);
-  uint64_t* wfull = bars;             // packed weights of stage s landed
-  uint64_t* bfull = bars + S_C;       // activation rows of stage s landed
-  uint64_t* empty = bars + 2 * S_C;   // the MMAs reading stage s finished
-  uint64_t* afull = bars + 3 * S_C;   // dequantised A stage in TMEM written
-  uint64_t* aempty = afull + S_A;     // the MMAs reading A stage finished
+  uint8_t* b_ring = base;                              // S_B x KS x [NT rows x 128 B], swizzled
+  uint8_t* w_ring = base + S_B * Cfg::kBBytes;         // S_W x KS x 4608-byte chunks
+  uint64_t* bars = reinterpret_cast<uint64_t*>(w_ring + S_W * Cfg::kWBytes);
+  uint64_t* wfull = bars;              // weight stage landed (TMA bytes)
+  uint64_t* wempty = wfull + S_W;      // weight stage read into registers (4 dequant warps)
+  uint64_t* bfull = wempty + S_W;      // activation stage landed
+  uint64_t* bempty = bfull + S_B;      // the MMAs reading the activation stage finished
+  uint64_t* afull = bempty + S_B;      // dequantised A stage in TMEM written (128 threads)
+  uint64_t* aempty = afull + S_A;      // the MMAs reading the A stage finished
   uint64_t* accfull = aempty + S_A;
   uint64_t* accempty = accfull + 2;
   uint64_t* drain = accempty + 2;
@@ -157,17 +204,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint32_t* tmem_slot = misc;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(misc + 2);
-  uint32_t* issued = misc + 3;
+  uint32_t* w_issued = misc + 3;
+  uint32_t* b_issued = misc + 4;
   int32_t* epi_rows = reinterpret_cast<int32_t*>(misc + 16);  // sorted_ids of the unit's block
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool gather = !a.a_sorted;
 
   if (tid == 0) {
-    for (int s = 0; s < S_C; ++s) {
+    for (int s = 0; s < S_W; ++s) {
       mbar_init(smem_u32(&wfull[s]), 1);
+      mbar_init(smem_u32(&wempty[s]), 4);
+    }
+    for (int s = 0; s < S_B; ++s) {
       mbar_init(smem_u32(&bfull[s]), gather ? kGatherThreads : 1);
-      mbar_init(smem_u32(&empty[s]), 1);
+      mbar_init(smem_u32(&bempty[s]), 1);
     }
     for (int s = 0; s < S_A; ++s) {
       mbar_init(smem_u32(&afull[s]), 128);
@@ -180,10 +231,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
     *last_flag = 0;
-    *issued = 0;
+    *w_issued = 0;
+    *b_issued = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0 && !gather) tma_prefetch_desc(&a.tmap_a);
+  if (warp == 2 && lane == 0 && !gather) tma_prefetch_desc(&a.tmap_a);
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -208,70 +260,43 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int64_t n_units = nblocks * a.n_tiles * split_k;
 
   if (warp == 0) {
-    // ---------------- producer: weight chunks (bulk TMA), sorted activation tiles (TMA) -------
+    // ---------------- weight producer: one bulk copy per stage, on a rotating lane ------------
+    // One thread's bulk copies are serviced one after another (about 300 ns each on GB300), so
+    // successive stages go to different lanes and many copies are in flight at once.
+    // Weights never depend on the previous kernel, so they stream before pdl_wait.
     const uint64_t policy = a.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
-    auto chunk_src = [&](const Unit& un, int kb) {
-      return a.wblob + kHeaderBytes +
-             ((static_cast<int64_t>(un.e) * a.n_tiles + un.jt) * a.n_kb + kb) * kChunkBytes;
-    };
-    // Weights never depend on the previous kernel: with routing already complete, stream the
-    // first S_C stages before waiting for the activations (programmatic dependent launch).
-    uint32_t pre = 0;
-    if (a.routing_ready) {
-      for (int64_t u = blockIdx.x; u < n_units && pre < static_cast<uint32_t>(S_C); u += gridDim.x) {
-        const Unit un = decode_unit(a, split_k, u);
-        if (!un.ok) continue;
-        for (int kb = un.kb0; kb < un.kb1 && pre < static_cast<uint32_t>(S_C); kb += KS, ++pre) {
-          const int nsub = min(KS, un.kb1 - kb);
-          if (lane == 0) {
-            const uint32_t wb = smem_u32(&wfull[pre]);
-            mbar_arrive_expect_tx(wb, nsub * kChunkBytes);
-            bulk_g2s(smem_u32(c_ring + pre * Cfg::kWBytes), chunk_src(un, kb), nsub * kChunkBytes,
-                     wb, policy);
-          }
-        }
-      }
-      __syncwarp();
-    }
-    pdl_wait();  // activations may be the previous kernel's output
     uint32_t it = 0;
     for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
       const Unit un = decode_unit(a, split_k, u);
       if (!un.ok) continue;
+      const uint8_t* strip = a.wblob + kHeaderBytes +
+                             ((static_cast<int64_t>(un.e) * a.n_tiles + un.jt) * a.n_kb) * kChunkBytes;
       for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
         const int nsub = min(KS, un.kb1 - kb);
-        const int s = it % S_C;
-        const uint32_t ph = (it / S_C) & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[s]), ph ^ 1, abort_flag, a.dev_err)))
-          goto producer_done;
-        if (lane == 0) {
-          if (it >= pre) {
-            const uint32_t wb = smem_u32(&wfull[s]);
-            mbar_arrive_expect_tx(wb, nsub * kChunkBytes);
-            bulk_g2s(smem_u32(c_ring + s * Cfg::kWBytes), chunk_src(un, kb), nsub * kChunkBytes,
-                     wb, policy);
-          }
-          if (!gather) {
-            const uint32_t bb = smem_u32(&bfull[s]);
-            mbar_arrive_expect_tx(bb, nsub * Cfg::kSubB);
-            for (int sb = 0; sb < nsub; ++sb)
-              tma_load_2d(smem_u32(b_ring + s * Cfg::kBBytes + sb * Cfg::kSubB), &a.tmap_a,
-                          (kb + sb) * kBlockK, static_cast<int>(un.b * a.block_m), bb);
-          }
+        const int s = it % S_W;
+        const uint32_t ph = (it / S_W) & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&wempty[s]), ph ^ 1, abort_flag, a.dev_err)))
+          goto wprod_done;
+        if (lane == static_cast<int>(it & 31)) {
+          const uint32_t wb = smem_u32(&wfull[s]);
+          mbar_arrive_expect_tx(wb, nsub * kChunkBytes);
+          bulk_g2s(smem_u32(w_ring + s * Cfg::kWBytes), strip + static_cast<int64_t>(kb) * kChunkBytes,
+                   nsub * kChunkBytes, wb, policy);
         }
         __syncwarp();
       }
     }
-  producer_done:
-    if (lane == 0) *issued = it > pre ? it : pre;
+  wprod_done:
+    if (lane == 0) *w_issued = it;
   } else if (warp == 2 || warp == 3) {
-    // ---------------- activation row gather (cp.async, 128-byte swizzled rows) ----------------
+    // ---------------- activation producer ----------------
+    pdl_wait();  // activations may be the previous kernel's output
+    uint32_t it = 0;
     if (gather) {
-      pdl_wait();  // activations may be the previous kernel's output
+      // rows gathered with 16-byte cp.async into the 128-byte-swizzled K-major layout
       const int g = tid - 64;
       const int c = g & 7;  // 16-byte chunk of a 128-byte row handled by this thread
       constexpr int R = NT / 8;  // rows per thread: (g >> 3) + 8j
-      uint32_t it = 0;
       for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
         const Unit un = decode_unit(a, split_k, u);
         if (!un.ok) continue;
@@ -283,9 +308,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
           const int nsub = min(KS, un.kb1 - kb);
-          const int s = it % S_C;
-          const uint32_t ph = (it / S_C) & 1;
-          if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, abort_flag, a.dev_err)) goto gather_done;
+          const int s = it % S_B;
+          const uint32_t ph = (it / S_B) & 1;
+          if (!mbar_wait(smem_u32(&bempty[s]), ph ^ 1, abort_flag, a.dev_err)) goto bprod_done;
           const uint32_t bdst = smem_u32(b_ring + s * Cfg::kBBytes);
           for (int sb = 0; sb < nsub; ++sb) {
 #pragma unroll
@@ -301,8 +326,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           cp_async_arrive_noinc(smem_u32(&bfull[s]));
         }
       }
-    gather_done:
+    bprod_done:
       cp_async_wait_all();
+    } else if (warp == 2) {
+      // rows already in sorted order: one 2-D TMA tile per K sub-block, rotating lanes
+      for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
+        const Unit un = decode_unit(a, split_k, u);
+        if (!un.ok) continue;
+        for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
+          const int nsub = min(KS, un.kb1 - kb);
+          const int s = it % S_B;
+          const uint32_t ph = (it / S_B) & 1;
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bempty[s]), ph ^ 1, abort_flag, a.dev_err)))
+            goto tprod_done;
+          const uint32_t bb = smem_u32(&bfull[s]);
+          if (lane == 0) mbar_arrive_expect_tx(bb, nsub * Cfg::kSubB);
+          __syncwarp();
+          for (int sb = 0; sb < nsub; ++sb)
+            if (lane == static_cast<int>((it * KS + sb) & 31))
+              tma_load_2d(smem_u32(b_ring + s * Cfg::kBBytes + sb * Cfg::kSubB), &a.tmap_a,
+                          (kb + sb) * kBlockK, static_cast<int>(un.b * a.block_m), bb);
+          __syncwarp();
+        }
+      }
+    tprod_done:
+      if (lane == 0) *b_issued = it;
     }
   } else if (warp == 1) {
     // ---------------- MMA issue: warp-wide loop, one elected lane issues ----------------
@@ -320,17 +368,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t d_tmem = tmem_base + ab * NT;
       for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
         const int nsub = min(KS, un.kb1 - kb);
-        const int s = it % S_C;
-        const uint32_t ph = (it / S_C) & 1;
+        const int sbi = it % S_B;
+        const uint32_t pb = (it / S_B) & 1;
         const int sa = it % S_A;
         const uint32_t pa = (it / S_A) & 1;
-        bool ok = mbar_wait(smem_u32(&bfull[s]), ph, abort_flag, a.dev_err);
-        ok = ok && mbar_wait(smem_u32(&afull[sa]), pa, abort_flag, a.dev_err);
+        bool ok = mbar_wait(smem_u32(&afull[sa]), pa, abort_flag, a.dev_err);
+        ok = ok && mbar_wait(smem_u32(&bfull[sbi]), pb, abort_flag, a.dev_err);
         if (!__all_sync(0xffffffffu, ok)) goto mma_done;
         if (gather) fence_proxy_async_smem();  // cp.async (generic proxy) rows -> tensor core
         tc_fence_after();
-        const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((s * Cfg::kBBytes) >> 4);
-        const uint32_t a_tmem = tmem_base + kACol0 + sa * (KS * 32);
+        const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((sbi * Cfg::kBBytes) >> 4);
+        const uint32_t a_tmem = tmem_base + Cfg::kACol0 + sa * (KS * 32);
         if (elect_one()) {
           for (int sb = 0; sb < nsub; ++sb) {
             const uint64_t bd = b_desc + static_cast<uint64_t>((sb * Cfg::kSubB) >> 4);
@@ -340,7 +388,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mma_ts(d_tmem, at + 16, bd + 4, idesc, 1u);
             mma_ts(d_tmem, at + 24, bd + 6, idesc, 1u);
           }
-          mma_commit(smem_u32(&empty[s]));
+          mma_commit(smem_u32(&bempty[sbi]));
           mma_commit(smem_u32(&aempty[sa]));
         }
         __syncwarp();
@@ -364,7 +412,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
       const Unit un = decode_unit(a, split_k, u);
       if (!un.ok) continue;
-      named_bar_epi();  // the previous unit's readers of epi_rows are done
+      named_bar_epi();  // the previous unit's readers of epi_rows / last_flag are done
       if (t < NT) epi_rows[t] = __ldg(a.sorted_ids + static_cast<int64_t>(un.b) * a.block_m + t);
       named_bar_epi();
       const int ab = lu & 1;
@@ -383,9 +431,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tc_fence_before();
             mbar_arrive(smem_u32(&accempty[ab]));
           }
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj)
-            store_column(a, un, t, c0 + jj, epi_rows[c0 + jj], __uint_as_float(r[jj]));
+          store_chunk16(a, un, t, c0, epi_rows, r);
         }
       } else {
         float* part = a.part + (un.tile * split_k + un.split) * (128 * NT);
@@ -409,10 +455,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           __threadfence();
           const float* tile_parts = a.part + un.tile * split_k * (128 * NT);
 #pragma unroll 1
-          for (int j = 0; j < NT; ++j) {
-            float v = 0.0f;
-            for (int s = 0; s < split_k; ++s) v += __ldcg(tile_parts + s * (128 * NT) + j * 128 + t);
-            store_column(a, un, t, j, epi_rows[j], v);
+          for (int c0 = 0; c0 < NT; c0 += 16) {
+            uint32_t r[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              float v = 0.0f;
+              for (int s = 0; s < split_k; ++s)
+                v += __ldcg(tile_parts + s * (128 * NT) + (c0 + jj) * 128 + t);
+              r[jj] = __float_as_uint(v);
+            }
+            store_chunk16(a, un, t, c0, epi_rows, r);
           }
           if (t == 0) a.cnt[un.tile] = 0;  // ready for the next call
         }
@@ -420,39 +472,48 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       ++lu;
     }
   } else if (warp >= 8) {
-    // ---------------- dequant warpgroups (stages alternate between the two) ----------------
+    // ---------------- dequant warpgroups (stages rotate over the groups) ----------------
     const int g = (warp - 8) >> 2;
     const int q = warp & 3;
     const int t = q * 32 + lane;
-    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kACol0;
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + Cfg::kACol0;
     uint32_t it = 0;
     for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
       const Unit un = decode_unit(a, split_k, u);
       if (!un.ok) continue;
       for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
-        if ((it & 1) != static_cast<uint32_t>(g)) continue;
+        if (it % kDqGroups != static_cast<uint32_t>(g)) continue;
         const int nsub = min(KS, un.kb1 - kb);
-        const int s = it % S_C;
-        const uint32_t ph = (it / S_C) & 1;
+        const int sw = it % S_W;
+        const uint32_t pw = (it / S_W) & 1;
         const int sa = it % S_A;
         const uint32_t pa = (it / S_A) & 1;
         // warp-uniform decisions: tcgen05.st below is a warp-collective instruction
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&wfull[s]), ph, abort_flag, a.dev_err)))
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&wfull[sw]), pw, abort_flag, a.dev_err)))
           goto dq_done;
-        for (int sb = 0; sb < nsub; ++sb) {
-          const uint8_t* ch = c_ring + s * Cfg::kWBytes + sb * kChunkBytes;
-          const uint4 lo = reinterpret_cast<const uint4*>(ch)[t];
-          const uint4 hi = reinterpret_cast<const uint4*>(ch + kCodeHalfBytes)[t];
-          const uint32_t s2 = reinterpret_cast<const uint32_t*>(ch + kScaleOffset)[t];
-          uint32_t v[32];
-          dequant_row64(lo, hi, s2, v);
-          if (sb == 0) {
-            if (!__all_sync(0xffffffffu,
-                            mbar_wait(smem_u32(&aempty[sa]), pa ^ 1, abort_flag, a.dev_err)))
-              goto dq_done;
-            tc_fence_after();
+        uint4 lo[KS], hi[KS];
+        uint32_t s2[KS];
+#pragma unroll
+        for (int sb = 0; sb < KS; ++sb) {
+          if (sb < nsub) {
+            const uint8_t* ch = w_ring + sw * Cfg::kWBytes + sb * kChunkBytes;
+            lo[sb] = reinterpret_cast<const uint4*>(ch)[t];
+            hi[sb] = reinterpret_cast<const uint4*>(ch + kCodeHalfBytes)[t];
+            s2[sb] = reinterpret_cast<const uint32_t*>(ch + kScaleOffset)[t];
           }
-          tmem_st32(lane_base + sa * (KS * 32) + sb * 32, v);
+        }
+        __syncwarp();  // every lane holds its rows: the weight stage may be refilled
+        if (lane == 0) mbar_arrive(smem_u32(&wempty[sw]));
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&aempty[sa]), pa ^ 1, abort_flag, a.dev_err)))
+          goto dq_done;
+        tc_fence_after();
+#pragma unroll
+        for (int sb = 0; sb < KS; ++sb) {
+          if (sb < nsub) {
+            uint32_t v[32];
+            dequant_row64(lo[sb], hi[sb], s2[sb], v);
+            tmem_st32(lane_base + sa * (KS * 32) + sb * 32, v);
+          }
         }
         tmem_wait_st();
         tc_fence_before();
@@ -465,11 +526,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   if (*abort_flag && warp == 0 && lane == 0) {
     // give in-flight copies a bounded chance to land before the CTA's memory goes away
-    const uint32_t n = *issued;
-    for (uint32_t j = (n > static_cast<uint32_t>(S_C) ? n - S_C : 0); j < n; ++j) {
-      mbar_wait_plain(smem_u32(&wfull[j % S_C]), (j / S_C) & 1);
-      if (!gather) mbar_wait_plain(smem_u32(&bfull[j % S_C]), (j / S_C) & 1);
-    }
+    const uint32_t nw = *w_issued, nb = *b_issued;
+    for (uint32_t j = (nw > static_cast<uint32_t>(S_W) ? nw - S_W : 0); j < nw; ++j)
+      mbar_wait_plain(smem_u32(&wfull[j % S_W]), (j / S_W) & 1);
+    if (!gather)
+      for (uint32_t j = (nb > static_cast<uint32_t>(S_B) ? nb - S_B : 0); j < nb; ++j)
+        mbar_wait_plain(smem_u32(&bfull[j % S_B]), (j / S_B) & 1);
   }
   tc_fence_before();
   __syncthreads();
@@ -483,16 +545,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // Host side: planner, tensor maps and launcher.
 // ------------------------------------------------------------------------------------------
 
-// Stage depth per block_m: two 64-wide K sub-blocks per stage for the weight-bound small
-// blocks, one for the larger blocks (shared memory then goes to activation tiles).
-template <int NT> struct StageK { static constexpr int value = NT <= 32 ? 2 : 1; };
+// Stage depth: the MMA warp pays a fixed cost of a few hundred cycles per burst of MMAs on top
+// of ~13 cycles per MMA, so the small-N (weight-bound) blocks issue 16 MMAs per stage (four
+// 64-wide K blocks, 18432-byte weight copies); larger blocks keep two (TMEM and activation
+// tiles then bound the stage size).
+template <int NT> struct StageK { static constexpr int value = NT <= 32 ? 4 : 2; };
 
 int stages_for_block_m(int block_m) {
   switch (block_m) {
-    case 16: return GemmCfg<16, StageK<16>::value>::kStages;
-    case 32: return GemmCfg<32, StageK<32>::value>::kStages;
-    case 64: return GemmCfg<64, StageK<64>::value>::kStages;
-    case 128: return GemmCfg<128, StageK<128>::value>::kStages;
+    case 16: return GemmCfg<16, StageK<16>::value>::kWStages;
+    case 32: return GemmCfg<32, StageK<32>::value>::kWStages;
+    case 64: return GemmCfg<64, StageK<64>::value>::kWStages;
+    case 128: return GemmCfg<128, StageK<128>::value>::kWStages;
     default: return 0;
   }
 }
