@@ -131,7 +131,8 @@ w4a16_status_t w4a16_pack_weights(const int32_t* qweight, const uint16_t* scales
  * zeros).  Rows of C not named are left untouched.  With W4A16_C_FP32 (epilogue NONE only)
  * C holds the FP32 sums unrounded (float, row stride ldc elements).
  * A  device BF16 [rows, K] with row stride lda elements (lda % 8 == 0, 16-byte aligned rows).
- * C  device BF16 with row stride ldc elements; N columns (epilogue NONE) or N/2 columns
+ * C  device BF16 (16-byte aligned, ldc % 8 == 0; FP32: ldc % 4 == 0) with row stride ldc
+ *    elements; N columns (epilogue NONE) or N/2 columns
  *    (epilogue SILU_MUL: C[., j] = bf16(silu(g) * u), g and u the BF16-rounded gate and up
  *    outputs; needs a W4A16_PACK_GATE_UP_PAIRED weight).
  * workspace  device scratch of w4a16_gemm_workspace_size() bytes, 256-byte aligned; its

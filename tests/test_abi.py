@@ -66,16 +66,14 @@ def test_block_m_planner():
     assert lib.plan_block_m(16384, 8, 48, 384) == 128
 
 
-def test_split_k_planner_prefers_splits_only_when_tiles_are_scarce():
-    # decode: 8 routed rows over 128 experts -> ~8 blocks x 12 tiles: too few for 148 SMs
+def test_gemm_planner_grid_and_split():
+    # decode: 8 routed rows over 128 experts -> ~8 blocks x 12 tiles = 96 units, one CTA each
     p = lib.plan_gemm(8, 128, 1536, 2048, 16, num_sms=148)
-    assert p["split_k"] > 1 and p["num_ctas"] <= 148
-    # prefill: thousands of tiles, no split
+    assert p["split_k"] == 1 and p["num_ctas"] == 96 and p["est_units"] == 96
+    # prefill: thousands of tiles, a persistent grid of one CTA per SM
     p = lib.plan_gemm(32768, 128, 1536, 2048, 128, num_sms=148)
     assert p["split_k"] == 1 and p["num_ctas"] == 148
-    # the split never exceeds half the K blocks
-    p = lib.plan_gemm(1, 384, 512, 256, 16, num_sms=148)
-    assert p["split_k"] <= 2
+    assert p["stages"] >= 4
     with pytest.raises(lib.LibraryError):
         lib.plan_gemm(8, 128, 1536, 2000, 16, num_sms=148)
 

@@ -187,6 +187,8 @@ static w4a16_status_t run_gemm(const GemmCall& c, const DeviceFacts& dev, cudaSt
     return fail(W4A16_INVALID_ARG, "unknown epilogue %d", c.epilogue);
   }
   if (c.ldc < out_cols) return fail(W4A16_INVALID_ARG, "ldc smaller than the output width");
+  if (reinterpret_cast<uintptr_t>(c.C) % 16 || c.ldc % ((c.row_flags & W4A16_C_FP32) ? 4 : 8))
+    return fail(W4A16_INVALID_ARG, "C must be 16-byte aligned with 16-byte aligned rows");
   if ((c.row_flags & W4A16_C_FP32) && c.epilogue != W4A16_EPILOGUE_NONE)
     return fail(W4A16_INVALID_ARG, "FP32 output is available with epilogue NONE only");
   if (R->capacity == 0 || c.W->E == 0) return W4A16_OK;

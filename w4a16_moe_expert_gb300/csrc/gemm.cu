@@ -37,7 +37,8 @@ namespace w4a16 {
 constexpr int kDqGroups = 2;  // dequant warpgroups; stage it goes to group it % kDqGroups
 constexpr int kGemmThreads = 256 + 128 * kDqGroups;
 constexpr int kTmemCols = 512;
-constexpr int kSmemBudget = 224 * 1024;
+constexpr int kSmemBudget = 216 * 1024;
+constexpr int kEpiStageBytes = 16 * 32 * 4;  // per epilogue warp: 16 tokens x 32 rows x 4 B
 constexpr int kGatherThreads = 64;  // warps 2 and 3 gather activation rows with cp.async
 
 // NT = block_m = MMA N; KS = 64-wide K sub-blocks per pipeline stage (one weight copy of
@@ -66,7 +67,7 @@ struct GemmCfg {
   static constexpr int kBarBytes = (2 * kWStages + 2 * kBStages + 2 * kAStages + 5) * 8;
   static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kBStages) * kBBytes +
                                        static_cast<size_t>(kWStages) * kWBytes + kBarBytes + 64 +
-                                       NT * 4;
+                                       NT * 4 + 16 + 4 * kEpiStageBytes;
   static_assert(NT % 16 == 0 && NT >= 16 && NT <= 128, "MMA N must be 16..128 in steps of 16");
   static_assert(kACol0 + 32 * KS * kAStages <= kTmemCols, "A stages must fit in TMEM");
   static_assert(kAStages >= 2, "A ring too shallow");
@@ -116,66 +117,70 @@ __device__ __forceinline__ float bf16_round(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
 }
 
-// Store one accumulator column (token column j of the block) for tile row t; `slot` is
-// sorted_ids at that position.  Epilogue NONE only.
-__device__ __forceinline__ void store_column(const GemmArgs& a, const Unit& un, int t, int j,
-                                             int32_t slot, float v) {
-  const bool routed = (slot >= 0 && slot < a.total_slots);
-  int64_t row;
-  if (a.c_sorted) {
-    row = static_cast<int64_t>(un.b) * a.block_m + j;  // padding rows are written too, as zeros
-  } else {
-    if (!routed) return;
-    row = slot;
-  }
-  const int n = tile_row_to_canonical(un.jt, t, a.N, a.paired != 0);
-  const float val = routed ? v : 0.0f;
-  if (a.c_f32)
-    reinterpret_cast<float*>(a.C)[row * a.ldc + n] = val;
-  else
-    a.C[row * a.ldc + n] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+// Output row of token column j of the unit's block, or -1 when nothing is written there.
+__device__ __forceinline__ int64_t out_row(const GemmArgs& a, const Unit& un, int j, int32_t slot) {
+  if (a.c_sorted) return static_cast<int64_t>(un.b) * a.block_m + j;  // padding rows get zeros
+  return (slot >= 0 && slot < a.total_slots) ? slot : -1;
 }
 
-// SiLU-and-mul for token columns j (even) and j + 1 of a paired gate/up tile.  Lane l < 16
-// holds gate rows and lane l + 16 the matching up rows; after one exchange lane l computes
-// column j and lane l + 16 column j + 1, so every lane does useful work.
-__device__ __forceinline__ void store_silu_pair(const GemmArgs& a, const Unit& un, int t, int j,
-                                                int32_t slot0, int32_t slot1, float v0, float v1) {
-  const int l = t & 31;
-  const bool hi = l >= 16;
-  // lanes < 16 send their column j+1 gate to lane + 16; lanes >= 16 send their column j up
-  const float send = hi ? v0 : v1;
-  const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-  const float g = bf16_round(hi ? recv : v0);
-  const float u = bf16_round(hi ? v1 : recv);
-  const int jj = hi ? j + 1 : j;
-  const int32_t slot = hi ? slot1 : slot0;
+// Writes token columns [c0, c0 + 16) of this warp's 32 tile rows (lanes) to C.  The values go
+// through the warp's staging area so that each lane ends up with consecutive output columns of
+// one token row and stores them with 16-byte vector stores (lane l: token l / 2, half l % 2).
+__device__ __forceinline__ void store_chunk16(const GemmArgs& a, const Unit& un, int q, int lane,
+                                              int c0, const int32_t* rows,
+                                              const uint32_t (&r)[16], uint8_t* stage) {
+  const int tok = lane >> 1, half = lane & 1;
+  const int32_t slot = rows[c0 + tok];
   const bool routed = (slot >= 0 && slot < a.total_slots);
-  int64_t row;
-  if (a.c_sorted) {
-    row = static_cast<int64_t>(un.b) * a.block_m + jj;
-  } else {
-    if (!routed) return;
-    row = slot;
-  }
-  const float h = routed ? __fdividef(g, 1.0f + __expf(-g)) * u : 0.0f;
-  const int col = 64 * un.jt + 16 * (t >> 5) + (l & 15);
-  a.C[row * a.ldc + col] = __bfloat16_as_ushort(__float2bfloat16_rn(h));
-}
-
-// All NT columns of one accumulator chunk of 16 (registers r) starting at column c0.
-__device__ __forceinline__ void store_chunk16(const GemmArgs& a, const Unit& un, int t, int c0,
-                                              const int32_t* rows, const uint32_t (&r)[16]) {
+  const int64_t row = out_row(a, un, c0 + tok, slot);
   if (a.epilogue == W4A16_EPILOGUE_SILU_MUL) {
+    // Lane l < 16 holds gate rows and lane l + 16 the matching up rows.  For each pair of
+    // tokens (j, j + 1) one exchange lets lane l compute token j and lane l + 16 token j + 1.
+    uint16_t* st = reinterpret_cast<uint16_t*>(stage);  // [16 tokens][16 columns]
+    const bool hi = lane >= 16;
 #pragma unroll
-    for (int jj = 0; jj < 16; jj += 2)
-      store_silu_pair(a, un, t, c0 + jj, rows[c0 + jj], rows[c0 + jj + 1], __uint_as_float(r[jj]),
-                      __uint_as_float(r[jj + 1]));
+    for (int jj = 0; jj < 16; jj += 2) {
+      const float v0 = __uint_as_float(r[jj]), v1 = __uint_as_float(r[jj + 1]);
+      const float recv = __shfl_xor_sync(0xffffffffu, hi ? v0 : v1, 16);
+      const float g = bf16_round(hi ? recv : v0);
+      const float u = bf16_round(hi ? v1 : recv);
+      const float h = __fdividef(g, 1.0f + __expf(-g)) * u;
+      st[(jj + (hi ? 1 : 0)) * 16 + (lane & 15)] = __bfloat16_as_ushort(__float2bfloat16_rn(h));
+    }
+    __syncwarp();
+    if (row >= 0) {
+      uint4 v = reinterpret_cast<const uint4*>(st)[tok * 2 + half];
+      if (!routed) v = make_uint4(0, 0, 0, 0);
+      const int col = 64 * un.jt + 16 * q + 8 * half;
+      *reinterpret_cast<uint4*>(a.C + row * a.ldc + col) = v;
+    }
   } else {
+    float* st = reinterpret_cast<float*>(stage);  // [16 tokens][32 rows]
 #pragma unroll
-    for (int jj = 0; jj < 16; ++jj)
-      store_column(a, un, t, c0 + jj, rows[c0 + jj], __uint_as_float(r[jj]));
+    for (int jj = 0; jj < 16; ++jj) st[jj * 32 + lane] = __uint_as_float(r[jj]);
+    __syncwarp();
+    if (row >= 0) {
+      const int col = tile_row_to_canonical(un.jt, 32 * q + 16 * half, a.N, a.paired != 0);
+      const float4* src = reinterpret_cast<const float4*>(st + tok * 32 + 16 * half);
+      if (a.c_f32) {
+        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.C) + row * a.ldc + col);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dst[k] = routed ? src[k] : make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        uint4* dst = reinterpret_cast<uint4*>(a.C + row * a.ldc + col);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const float4 x = src[2 * k], y = src[2 * k + 1];
+          auto pk = [&](float lo, float hi2) {
+            return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(routed ? lo : 0.f))) |
+                   (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(routed ? hi2 : 0.f))) << 16);
+          };
+          dst[k] = make_uint4(pk(x.x, x.y), pk(x.z, x.w), pk(y.x, y.y), pk(y.z, y.w));
+        }
+      }
+    }
   }
+  __syncwarp();  // the staging area is reused by the next chunk
 }
 
 template <int NT, int KS>
@@ -207,6 +212,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint32_t* w_issued = misc + 3;
   uint32_t* b_issued = misc + 4;
   int32_t* epi_rows = reinterpret_cast<int32_t*>(misc + 16);  // sorted_ids of the unit's block
+  // per-epilogue-warp staging for vectorised stores (16-byte aligned)
+  uint8_t* epi_stage_base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(epi_rows + NT) + 15) & ~static_cast<uintptr_t>(15));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool gather = !a.a_sorted;
@@ -408,6 +416,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     pdl_wait();  // outputs may still be read by the previous kernel
     const int q = warp - 4;
     const int t = q * 32 + lane;  // tile row = TMEM lane
+    uint8_t* epi_stage = epi_stage_base + q * kEpiStageBytes;
     uint32_t lu = 0;
     for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
       const Unit un = decode_unit(a, split_k, u);
@@ -422,16 +431,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ab * NT;
       if (split_k == 1) {
+        // TMEM loads are double-buffered: the next 16 columns are in flight while the current
+        // ones are converted and stored.
+        uint32_t r0[16], r1[16];
+        tmem_ld16(taddr, r0);
 #pragma unroll 1
-        for (int c0 = 0; c0 < NT; c0 += 16) {
-          uint32_t r[16];
-          tmem_ld16(taddr + c0, r);
-          tmem_wait_ld();
+        for (int c0 = 0; c0 < NT; c0 += 32) {
+          tmem_wait_ld16(r0);
+          if (c0 + 16 < NT) tmem_ld16(taddr + c0 + 16, r1);
           if (c0 + 16 >= NT) {
             tc_fence_before();
             mbar_arrive(smem_u32(&accempty[ab]));
           }
-          store_chunk16(a, un, t, c0, epi_rows, r);
+          store_chunk16(a, un, q, lane, c0, epi_rows, r0, epi_stage);
+          if (c0 + 16 < NT) {
+            tmem_wait_ld16(r1);
+            if (c0 + 32 < NT) tmem_ld16(taddr + c0 + 32, r0);
+            if (c0 + 32 >= NT) {
+              tc_fence_before();
+              mbar_arrive(smem_u32(&accempty[ab]));
+            }
+            store_chunk16(a, un, q, lane, c0 + 16, epi_rows, r1, epi_stage);
+          }
         }
       } else {
         float* part = a.part + (un.tile * split_k + un.split) * (128 * NT);
@@ -439,7 +460,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int c0 = 0; c0 < NT; c0 += 16) {
           uint32_t r[16];
           tmem_ld16(taddr + c0, r);
-          tmem_wait_ld();
+          tmem_wait_ld16(r);
           if (c0 + 16 >= NT) {
             tc_fence_before();
             mbar_arrive(smem_u32(&accempty[ab]));
@@ -464,7 +485,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 v += __ldcg(tile_parts + s * (128 * NT) + (c0 + jj) * 128 + t);
               r[jj] = __float_as_uint(v);
             }
-            store_chunk16(a, un, t, c0, epi_rows, r);
+            store_chunk16(a, un, q, lane, c0, epi_rows, r, epi_stage);
           }
           if (t == 0) a.cnt[un.tile] = 0;  // ready for the next call
         }
@@ -580,7 +601,11 @@ void plan_gemm(int total_slots, int E, int N, int K, int block_m, int rows_per_e
   const double units1 = std::max(1.0, std::ceil(blocks)) * n_tiles;
   const double W = static_cast<double>(n_kb) * kChunkBytes;
   const double R = 2.0 * 128 * block_m * 4;
-  const int s_max = std::max(1, std::min(16, n_kb / 2));
+  // K splits measured slower than unsplit units at every decode size on GB300 (the partial
+  // round trip and the extra per-unit pipeline ramp outweigh the added parallelism), so the
+  // planner keeps one split; the schedule override still exercises the split path.
+  const int s_max = 1;
+  (void)n_kb;
   int best_s = 1;
   double best = 1e300;
   for (int s = 1; s <= s_max; ++s) {
