@@ -5,8 +5,9 @@ gate_up [128, 1536, 2048], down [128, 2048, 768], uint4 group-32 BF16 scales),
 seeded synthetic inputs, token sweep T in {1, 8, 64, 512, 4096}.
 
 One step = one pass of the whole path for every T of the sweep: align, gate_up
-with fused SiLU-and-mul, down, top-k weighted sum, each a C-ABI call on the
-current stream with CUDA events between them.  L2 is flushed (a 512 MB memset,
+(activation-row gather, then the GEMM with fused SiLU-and-mul), down, top-k
+weighted sum, each a C-ABI call on the current stream with CUDA events between
+the four stages; the step is captured once as a CUDA graph and replayed.  L2 is flushed (a 512 MB memset,
 outside the events) before every T, so weights and activations come from HBM.
 
 value = weight HBM GB/s over the sweep: sum of the packed weight bytes the two
@@ -75,6 +76,7 @@ def accounting(wl, T, topk_ids):
     for d in (gu, dn):
         d["bytes"] = d["weight_bytes"] + d["act_bytes"] + d["out_bytes"]
     return {"T": T, "T_r": T_r, "E_act": e_act, "gate_up": gu, "down": dn}
+
 
 
 # ---- clock sampling -------------------------------------------------------------------------
@@ -164,6 +166,7 @@ def run_ours(args, rank, world, local_rank):
             "sorted": torch.empty(cap, dtype=torch.int32, device=dev),
             "expert": torch.empty(cap // bm, dtype=torch.int32, device=dev),
             "ntp": torch.empty(1, dtype=torch.int32, device=dev),
+            "xs": torch.empty((cap, wl.H), dtype=torch.bfloat16, device=dev),
             "h": torch.empty((cap, wl.I), dtype=torch.bfloat16, device=dev),
             "y": torch.empty((T * wl.top_k, wl.H), dtype=torch.float32, device=dev),
             "out": torch.empty((T, wl.H), dtype=torch.bfloat16, device=dev),
@@ -188,9 +191,17 @@ def run_ours(args, rank, world, local_rank):
             lib._ptr(c["expert"]), lib._ptr(c["ntp"]), c["cap"], 0, None, lib._stream())
         if ev:
             ev[1].record()
-        lib.moe_gemm(c["x"], wl.top_k, w13, r, epilogue=lib.EPILOGUE_SILU_MUL,
-                     row_flags=lib.C_ROWS_SORTED, out=c["h"], workspace=c["ws"],
-                     expected_rows_per_expert=rows_hint[c["T"]])
+        # gate_up stage (as the layer call runs it): large blocks gather the activation rows into
+        # aligned order first and read them by TMA; small blocks gather inside the GEMM
+        if c["block_m"] >= 64:
+            lib.gather_rows(c["x"], wl.top_k, r, out=c["xs"])
+            lib.moe_gemm(c["xs"], 1, w13, r, epilogue=lib.EPILOGUE_SILU_MUL,
+                         row_flags=lib.A_ROWS_SORTED | lib.C_ROWS_SORTED, out=c["h"],
+                         workspace=c["ws"], expected_rows_per_expert=rows_hint[c["T"]])
+        else:
+            lib.moe_gemm(c["x"], wl.top_k, w13, r, epilogue=lib.EPILOGUE_SILU_MUL,
+                         row_flags=lib.C_ROWS_SORTED, out=c["h"], workspace=c["ws"],
+                         expected_rows_per_expert=rows_hint[c["T"]])
         if ev:
             ev[2].record()
         lib.moe_gemm(c["h"], 1, w2, r, row_flags=lib.A_ROWS_SORTED | lib.C_FP32, out=c["y"],
@@ -345,7 +356,7 @@ def run_ours(args, rank, world, local_rank):
         },
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": 4 * len(cases) * args.steps,
+        "gpu_launches": sum(5 if c["block_m"] >= 64 else 4 for c in cases) * args.steps,
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -174,6 +174,18 @@ w4a16_status_t w4a16_moe_gemm(const uint16_t* A, int64_t lda, int a_row_div,
                               int32_t* dev_err, w4a16_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Activation rows in aligned order (the gather of "Two kernel families": indexed kernels read
+ * token rows through sorted_ids).  out[p, :] = x[sorted_ids[p] / a_row_div, :] for every
+ * routed position p < *num_tokens_padded; padding rows and rows past num_tokens_padded are
+ * not written.  x device BF16 [rows, K] (row stride ldx), out device BF16 [capacity, K] (row
+ * stride ldo); K % 8 == 0, ldx % 8 == 0, ldo % 8 == 0, both 16-byte aligned.  The result
+ * feeds w4a16_moe_gemm with W4A16_A_ROWS_SORTED (activation tiles by 2-D TMA).
+ * ---------------------------------------------------------------------------------------- */
+w4a16_status_t w4a16_gather_rows(const uint16_t* x, int64_t ldx, int K, int a_row_div,
+                                 const w4a16_routing_t* routing, uint16_t* out, int64_t ldo,
+                                 w4a16_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * Top-k weighted sum (the "top-K expert output merge" of the humans& page).
  * Y device FP32 [T*top_k, H] (the per-slot down outputs, unrounded); out[t, :] =
  * bf16(sum over s ascending with topk_ids[t,s] >= 0 of topk_weights[t,s] * Y[t*top_k + s, :]),
@@ -184,8 +196,8 @@ w4a16_status_t w4a16_topk_sum(const float* Y, const int32_t* topk_ids,
                               uint16_t* out, w4a16_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
- * Whole layer: align -> gate_up (SiLU-and-mul fused) -> down -> top-k sum, four kernels
- * chained with programmatic dependent launch ("humans& ...", "Blackwell hides the conversion
+ * Whole layer: align -> row gather -> gate_up (SiLU-and-mul fused) -> down -> top-k sum, five
+ * kernels chained with programmatic dependent launch ("humans& ...", "Blackwell hides the conversion
  * work": FC2 starts its weight work before FC1 completes).
  * x  device BF16 [T, H]; w13 packed [E, 2I, H] with W4A16_PACK_GATE_UP_PAIRED; w2 packed
  * [E, H, I]; topk_ids / topk_weights device [T, top_k]; out device BF16 [T, H] (a token

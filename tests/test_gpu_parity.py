@@ -207,6 +207,19 @@ def test_gemm_sorted_rows_modes(lib):
     assert_close_bf16(C2.cpu()[rows], ref[rows], "A rows sorted")
 
 
+def test_gather_rows_bit_exact_and_sorted_gemm(lib):
+    qw, sc, x, ids, W, r, (s, e, ntp) = _gemm_case(lib, 50, 4, 8, 256, 512, 32, 33)
+    xs = lib.gather_rows(x.to(DEV), 4, r).cpu()
+    for p in range(ntp):
+        i = int(s[p])
+        if i < 200:
+            assert torch.equal(bits(xs[p]), bits(x[i // 4]))
+    C = lib.moe_gemm(xs.to(DEV), 1, W, r, row_flags=lib.A_ROWS_SORTED)
+    ref = oracle.moe_gemm(x, 4, qw, sc, s, e, ntp, 32, 200)
+    rows = routed_rows(ids)
+    assert_close_bf16(C.cpu()[rows], ref[rows], "gathered + sorted-row GEMM")
+
+
 def test_gemm_edge_cases(lib):
     E, N, K = 4, 128, 128
     qw, sc = workloads.draw_weights(E, N, K, seed=41)

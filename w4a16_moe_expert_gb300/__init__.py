@@ -23,7 +23,7 @@ from . import build as _build
 
 __all__ = [
     "load", "library_path", "align_capacity", "moe_align", "PackedWeights", "pack_weights",
-    "Routing", "moe_gemm", "topk_sum", "moe_layer", "layer_workspace_size", "plan_block_m",
+    "Routing", "moe_gemm", "gather_rows", "topk_sum", "moe_layer", "layer_workspace_size", "plan_block_m",
     "plan_gemm", "debug_dequant", "gemm_workspace_size", "EPILOGUE_NONE", "EPILOGUE_SILU_MUL",
     "A_ROWS_SORTED", "C_ROWS_SORTED", "C_FP32", "PACK_GATE_UP_PAIRED", "LibraryError",
 ]
@@ -90,6 +90,7 @@ _SIGNATURES = {
     "w4a16_moe_gemm": (_I32, [_VP, _I64, _I32, _P(PackedDesc), _P(RoutingDesc), _I32, _U32, _VP, _I64,
                               _VP, _SZ, _I32, _P(ScheduleDesc), _VP, _VP]),
     "w4a16_topk_sum": (_I32, [_VP, _VP, _VP, _I32, _I32, _I32, _VP, _VP]),
+    "w4a16_gather_rows": (_I32, [_VP, _I64, _I32, _I32, _P(RoutingDesc), _VP, _I64, _VP]),
     "w4a16_plan_block_m": (_I32, [_I32, _I32, _I32, _I32]),
     "w4a16_layer_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32, _I32]),
     "w4a16_moe_layer": (_I32, [_VP, _P(PackedDesc), _P(PackedDesc), _VP, _VP, _I32, _I32, _I32, _I32,
@@ -280,6 +281,20 @@ def moe_gemm(A: torch.Tensor, a_row_div: int, W: PackedWeights, routing: Routing
         _ptr(A), A.stride(0), a_row_div, ctypes.byref(W.desc), ctypes.byref(rd), epilogue, row_flags,
         _ptr(out), out.stride(0), _ptr(workspace), workspace.numel(), expected_rows_per_expert,
         ctypes.byref(sched), _ptr(dev_err), _stream()))
+    return out
+
+
+def gather_rows(x: torch.Tensor, a_row_div: int, routing: Routing,
+                out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Activation rows in aligned order: out[p] = x[sorted_ids[p] // a_row_div] (routed p)."""
+    _cuda(x, torch.bfloat16, "x")
+    K = x.shape[1]
+    if out is None:
+        out = torch.zeros((routing.capacity, K), dtype=torch.bfloat16, device=x.device)
+    _cuda(out, torch.bfloat16, "out")
+    rd = routing.desc()
+    _check("w4a16_gather_rows", load().w4a16_gather_rows(
+        _ptr(x), x.stride(0), K, a_row_div, ctypes.byref(rd), _ptr(out), out.stride(0), _stream()))
     return out
 
 

@@ -138,6 +138,57 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
   if (tid == 0 && bad_id) set_dev_err(dev_err, W4A16_DEVERR_BAD_EXPERT_ID);
 }
 
+// Activation rows in aligned order: out[p, :] = x[sorted_ids[p] / a_row_div, :] for every
+// routed position p < num_tokens_padded (padding rows are left as they are).  One warp per
+// row, 16-byte vectors; lets the GEMM stream activation tiles with 2-D TMA instead of gathering
+// rows itself.
+__global__ void __launch_bounds__(256)
+    gather_rows_kernel(const uint16_t* __restrict__ x, int64_t ldx, int K, int a_row_div,
+                       const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ ntp_ptr,
+                       int total_slots, int64_t capacity, uint16_t* __restrict__ out,
+                       int64_t ldo) {
+  pdl_wait();  // routing comes from the align kernel
+  // The dependent GEMM reads the routing before its own wait, so it may only start once the
+  // routing is known to be complete, i.e. after the wait above.
+  pdl_launch_dependents();
+  int64_t ntp = *ntp_ptr;
+  if (ntp < 0) ntp = 0;
+  if (ntp > capacity) ntp = capacity;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int vec = K / 8;  // 16-byte vectors per row
+  for (int64_t p = warp0; p < ntp; p += nwarps) {
+    const int32_t i = __ldg(sorted_ids + p);
+    if (i < 0 || i >= total_slots) continue;
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(i / a_row_div) * ldx);
+    uint4* dst = reinterpret_cast<uint4*>(out + p * ldo);
+    for (int v = lane; v < vec; v += 32) dst[v] = __ldg(src + v);
+  }
+}
+
+cudaError_t launch_gather_rows(const uint16_t* x, int64_t ldx, int K, int a_row_div,
+                               const int32_t* sorted_ids, const int32_t* ntp, int total_slots,
+                               int64_t capacity, uint16_t* out, int64_t ldo, int num_sms,
+                               cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  const int64_t max_rows = capacity < total_slots ? capacity : total_slots;
+  int64_t blocks = (max_rows + 7) / 8;  // 8 warps (rows) per block
+  const int64_t cap_blocks = static_cast<int64_t>(num_sms) * 8;
+  if (blocks > cap_blocks) blocks = cap_blocks;
+  if (blocks < 1) blocks = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gather_rows_kernel, x, ldx, K, a_row_div, sorted_ids, ntp,
+                            total_slots, capacity, out, ldo);
+}
+
 size_t align_smem_bytes(int E) {
   return static_cast<size_t>(kAlignWarps * E + E + 1) * sizeof(int32_t);
 }

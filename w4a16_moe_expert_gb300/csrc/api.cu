@@ -17,6 +17,10 @@ cudaError_t launch_moe_align(const int32_t* topk_ids, int n_slots, int E, int bl
                              int64_t capacity, int validate, int32_t* dev_err,
                              int32_t* zero_words, int n_zero_words, cudaStream_t stream);
 size_t align_smem_bytes(int E);
+cudaError_t launch_gather_rows(const uint16_t* x, int64_t ldx, int K, int a_row_div,
+                               const int32_t* sorted_ids, const int32_t* ntp, int total_slots,
+                               int64_t capacity, uint16_t* out, int64_t ldo, int num_sms,
+                               cudaStream_t stream);
 cudaError_t launch_pack(const int32_t* qweight, const uint16_t* scales, int E, int N, int K,
                         uint32_t flags, void* packed, cudaStream_t stream);
 cudaError_t launch_debug_dequant(const void* packed, int e, int N, int K, uint32_t flags,
@@ -368,6 +372,26 @@ w4a16_status_t w4a16_moe_gemm(const uint16_t* A, int64_t lda, int a_row_div,
   return run_gemm(c, dev, stream);
 }
 
+w4a16_status_t w4a16_gather_rows(const uint16_t* x, int64_t ldx, int K, int a_row_div,
+                                 const w4a16_routing_t* routing, uint16_t* out, int64_t ldo,
+                                 w4a16_stream_t stream) {
+  const w4a16_routing_t* R = routing;
+  if (!R || !R->sorted_ids || !R->num_tokens_padded || !x || !out)
+    return fail(W4A16_INVALID_ARG, "NULL pointer");
+  if (K <= 0 || K % 8 || ldx % 8 || ldo % 8 || ldx < K || ldo < K || a_row_div <= 0 ||
+      reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(out) % 16)
+    return fail(W4A16_INVALID_ARG, "need K, ldx, ldo multiples of 8 and 16-byte aligned rows");
+  if (R->capacity < 0 || R->total_slots < 0) return fail(W4A16_INVALID_ARG, "bad routing sizes");
+  DeviceFacts dev;
+  w4a16_status_t st = device_facts(&dev);
+  if (st != W4A16_OK) return st;
+  if (R->capacity == 0 || R->total_slots == 0) return W4A16_OK;
+  cudaError_t err = launch_gather_rows(x, ldx, K, a_row_div, R->sorted_ids, R->num_tokens_padded,
+                                       R->total_slots, R->capacity, out, ldo, dev.num_sms, stream);
+  if (err != cudaSuccess) return cuda_fail(err, "gather_rows launch");
+  return W4A16_OK;
+}
+
 w4a16_status_t w4a16_topk_sum(const float* Y, const int32_t* topk_ids,
                               const float* topk_weights, int T, int top_k, int H,
                               uint16_t* out, w4a16_stream_t stream) {
@@ -406,11 +430,12 @@ w4a16_status_t w4a16_plan_gemm(int total_slots, int E, int N, int K, int block_m
 
 // Layer workspace, in order (each piece 256-byte aligned):
 //   sorted_ids [cap] | expert_ids [cap / bm] | ntp [1] | K-split counters | K-split partials |
+//   xs (gathered activations, sorted rows) [cap, H] BF16 |
 //   h (SiLU output, sorted rows) [cap, I] BF16 | Y (down output, slot rows) [T*top_k, H] FP32
 struct LayerLayout {
   int block_m;
   int64_t cap;
-  size_t off_sorted, off_expert, off_ntp, off_cnt, off_part, off_h, off_y, total;
+  size_t off_sorted, off_expert, off_ntp, off_cnt, off_part, off_xs, off_h, off_y, total;
 };
 
 static LayerLayout layer_layout(int T, int top_k, int E, int E_global, int H, int I, int block_m) {
@@ -428,6 +453,8 @@ static LayerLayout layer_layout(int T, int top_k, int E, int E_global, int H, in
   o = round_up(o + split_unit_budget(L.block_m) * 4, 256);
   L.off_part = o;
   o += kPartialBytes;
+  L.off_xs = o;  // gathered activations, used by large blocks only
+  o = round_up(o + (L.block_m >= 64 ? static_cast<size_t>(L.cap) * H * 2 : 0), 256);
   L.off_h = o;
   o = round_up(o + static_cast<size_t>(L.cap) * I * 2, 256);
   L.off_y = o;
@@ -475,6 +502,7 @@ w4a16_status_t w4a16_moe_layer(const uint16_t* x, const w4a16_packed_weights_t* 
   int32_t* sorted_ids = reinterpret_cast<int32_t*>(ws + L.off_sorted);
   int32_t* expert_ids = reinterpret_cast<int32_t*>(ws + L.off_expert);
   int32_t* ntp = reinterpret_cast<int32_t*>(ws + L.off_ntp);
+  uint16_t* xs = reinterpret_cast<uint16_t*>(ws + L.off_xs);
   uint16_t* h = reinterpret_cast<uint16_t*>(ws + L.off_h);
   float* y = reinterpret_cast<float*>(ws + L.off_y);
   const int n_slots = T * top_k;
@@ -488,12 +516,23 @@ w4a16_status_t w4a16_moe_layer(const uint16_t* x, const w4a16_packed_weights_t* 
   w4a16_routing_t R{sorted_ids, expert_ids, ntp, L.cap, L.block_m, n_slots};
   const int eg = E_global > 0 ? E_global : E;
   const int rows_hint = std::max(1, static_cast<int>(std::lround(static_cast<double>(n_slots) / eg)));
-  GemmCall g1{x, H, top_k, w13, &R, W4A16_EPILOGUE_SILU_MUL, W4A16_C_ROWS_SORTED, h, I,
-              ws + L.off_cnt, (L.off_h - L.off_cnt), rows_hint, nullptr, dev_err, 0};
+  // Large blocks (prefill) read activation tiles by 2-D TMA from rows gathered into aligned
+  // order by a separate kernel (the gate_up GEMM streams its first weights meanwhile); small
+  // blocks (decode) gather their few rows inside the GEMM, which saves a launch.
+  const bool pre_gather = L.block_m >= 64;
+  if (pre_gather) {
+    err = launch_gather_rows(x, H, H, top_k, sorted_ids, ntp, n_slots, L.cap, xs, H, dev.num_sms,
+                             stream);
+    if (err != cudaSuccess) return cuda_fail(err, "gather_rows launch");
+  }
+  GemmCall g1{pre_gather ? xs : x, H, pre_gather ? 1 : top_k, w13, &R, W4A16_EPILOGUE_SILU_MUL,
+              (pre_gather ? W4A16_A_ROWS_SORTED : 0u) | W4A16_C_ROWS_SORTED, h, I,
+              ws + L.off_cnt, (L.off_xs - L.off_cnt), rows_hint, nullptr, dev_err,
+              pre_gather ? 1 : 0};
   if ((st = run_gemm(g1, dev, stream)) != W4A16_OK) return st;
   GemmCall g2{h, I, 1, w2, &R, W4A16_EPILOGUE_NONE, W4A16_A_ROWS_SORTED | W4A16_C_FP32,
               reinterpret_cast<uint16_t*>(y), H,
-              ws + L.off_cnt, (L.off_h - L.off_cnt), rows_hint, nullptr, dev_err, 1};
+              ws + L.off_cnt, (L.off_xs - L.off_cnt), rows_hint, nullptr, dev_err, 1};
   if ((st = run_gemm(g2, dev, stream)) != W4A16_OK) return st;
   err = launch_topk_sum(y, topk_ids, topk_weights, T, top_k, H, out, stream);
   if (err != cudaSuccess) return cuda_fail(err, "topk_sum launch");
