@@ -186,6 +186,33 @@ w4a16_status_t w4a16_gather_rows(const uint16_t* x, int64_t ldx, int K, int a_ro
                                  w4a16_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Indexed GEMM that allocates nothing.  The paper has no counterpart: this entry point exists
+ * for callers that cannot hand the library a workspace, such as an inference-engine plugin
+ * whose enqueue hook receives only its input and output buffers, or a serving loop that must
+ * not call cudaMalloc after start-up (the call can synchronise the device and fragment memory
+ * budgeted up front).
+ *
+ * Same arguments and results as w4a16_moe_gemm without the workspace: the K-split scratch
+ * (arrival counters and FP32 partial sums) is a library-owned device array of
+ * W4A16_STATIC_SCRATCH_BYTES that every GPU loading the library keeps until the process
+ * exits.  The first call on a device looks up that array's device address (once per device,
+ * with the device current); make that first call before any stream capture.  Each call
+ * clears the counter words it needs with an asynchronous memset on `stream` and calls no
+ * cudaMalloc, cudaFree or other allocating routine.  All calls share the one array: calls
+ * whose kernels may overlap on the GPU (different streams, or concurrent host threads) race
+ * on it and must be serialised by the caller.  A problem that would need more scratch than
+ * the array holds is rejected with W4A16_WORKSPACE_TOO_SMALL.
+ * ---------------------------------------------------------------------------------------- */
+#define W4A16_STATIC_SCRATCH_BYTES ((size_t)16 * 1024 * 1024 + 8192)
+w4a16_status_t w4a16_moe_gemm_static_scratch(const uint16_t* A, int64_t lda, int a_row_div,
+                                             const w4a16_packed_weights_t* W,
+                                             const w4a16_routing_t* routing, int epilogue,
+                                             uint32_t row_flags, uint16_t* C, int64_t ldc,
+                                             int expected_rows_per_expert,
+                                             const w4a16_schedule_t* schedule, int32_t* dev_err,
+                                             w4a16_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * Top-k weighted sum (the "top-K expert output merge" of the humans& page).
  * Y device FP32 [T*top_k, H] (the per-slot down outputs, unrounded); out[t, :] =
  * bf16(sum over s ascending with topk_ids[t,s] >= 0 of topk_weights[t,s] * Y[t*top_k + s, :]),

@@ -91,6 +91,8 @@ _SIGNATURES = {
                               _VP, _SZ, _I32, _P(ScheduleDesc), _VP, _VP]),
     "w4a16_topk_sum": (_I32, [_VP, _VP, _VP, _I32, _I32, _I32, _VP, _VP]),
     "w4a16_gather_rows": (_I32, [_VP, _I64, _I32, _I32, _P(RoutingDesc), _VP, _I64, _VP]),
+    "w4a16_moe_gemm_static_scratch": (_I32, [_VP, _I64, _I32, _P(PackedDesc), _P(RoutingDesc), _I32,
+                                             _U32, _VP, _I64, _I32, _P(ScheduleDesc), _VP, _VP]),
     "w4a16_plan_block_m": (_I32, [_I32, _I32, _I32, _I32]),
     "w4a16_layer_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32, _I32]),
     "w4a16_moe_layer": (_I32, [_VP, _P(PackedDesc), _P(PackedDesc), _VP, _VP, _I32, _I32, _I32, _I32,
@@ -295,6 +297,30 @@ def gather_rows(x: torch.Tensor, a_row_div: int, routing: Routing,
     rd = routing.desc()
     _check("w4a16_gather_rows", load().w4a16_gather_rows(
         _ptr(x), x.stride(0), K, a_row_div, ctypes.byref(rd), _ptr(out), out.stride(0), _stream()))
+    return out
+
+
+def moe_gemm_static_scratch(A: torch.Tensor, a_row_div: int, W: PackedWeights, routing: Routing,
+                            epilogue: int = EPILOGUE_NONE, row_flags: int = 0,
+                            out: Optional[torch.Tensor] = None, expected_rows_per_expert: int = 0,
+                            split_k: int = 0, num_ctas: int = 0,
+                            dev_err: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The indexed GEMM for callers that cannot allocate: its K-split scratch is a device array
+    owned by the library (shared by all calls, so calls must not overlap on the GPU).  The
+    output tensor is the caller's; pass ``out`` to make the call allocate nothing at all."""
+    _cuda(A, torch.bfloat16, "A")
+    width = W.N // 2 if epilogue == EPILOGUE_SILU_MUL else W.N
+    if out is None:
+        rows = routing.capacity if row_flags & C_ROWS_SORTED else routing.total_slots
+        out = torch.zeros((rows, width), dtype=torch.float32 if row_flags & C_FP32 else torch.bfloat16,
+                          device=A.device)
+    _cuda(out, torch.float32 if row_flags & C_FP32 else torch.bfloat16, "out")
+    sched = ScheduleDesc(split_k, num_ctas)
+    rd = routing.desc()
+    _check("w4a16_moe_gemm_static_scratch", load().w4a16_moe_gemm_static_scratch(
+        _ptr(A), A.stride(0), a_row_div, ctypes.byref(W.desc), ctypes.byref(rd), epilogue, row_flags,
+        _ptr(out), out.stride(0), expected_rows_per_expert, ctypes.byref(sched), _ptr(dev_err),
+        _stream()))
     return out
 
 

@@ -38,6 +38,9 @@ static w4a16_status_t fail(w4a16_status_t st, const char* fmt, ...) {
   return st;
 }
 
+// Detail text for failures found outside this file.
+void set_error_detail(const char* text) { snprintf(g_detail, sizeof g_detail, "%s", text); }
+
 static w4a16_status_t cuda_fail(cudaError_t err, const char* what) {
   cudaGetLastError();  // clear the sticky-free launch error
   return fail(W4A16_CUDA_ERROR, "%s: %s", what, cudaGetErrorString(err));
