@@ -320,15 +320,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t ph = (it / S_B) & 1;
           if (!mbar_wait(smem_u32(&bempty[s]), ph ^ 1, abort_flag, a.dev_err)) goto bprod_done;
           const uint32_t bdst = smem_u32(b_ring + s * Cfg::kBBytes);
+          // Padding rows are not loaded: MMA column j reads only B row j, so whatever a
+          // padding row holds lands in a token column that the epilogue discards.
           for (int sb = 0; sb < nsub; ++sb) {
 #pragma unroll
             for (int j = 0; j < R; ++j) {
+              if (arow[j] < 0) continue;
               const int r = (g >> 3) + 8 * j;
               const uint32_t dst = bdst + sb * Cfg::kSubB + r * 128 + ((c ^ (r & 7)) << 4);
-              const uint16_t* src = arow[j] >= 0
-                                        ? a.A + static_cast<int64_t>(arow[j]) * a.lda + (kb + sb) * kBlockK + c * 8
-                                        : a.A;
-              cp_async_16(dst, src, arow[j] >= 0 ? 16u : 0u);
+              cp_async_16(dst, a.A + static_cast<int64_t>(arow[j]) * a.lda + (kb + sb) * kBlockK + c * 8, 16u);
             }
           }
           cp_async_arrive_noinc(smem_u32(&bfull[s]));
@@ -361,52 +361,62 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (lane == 0) *b_issued = it;
     }
   } else if (warp == 1) {
-    // ---------------- MMA issue: warp-wide loop, one elected lane issues ----------------
+    // ---------------- MMA issue: one elected thread runs the whole loop ----------------
+    // Measured on GB300: a burst of MMAs issued from a fully unrolled sequence inside one
+    // long-lived elected region costs ~9 cycles per N=16 MMA, while re-electing every stage or
+    // issuing from a rolled loop costs several hundred cycles per stage.
     constexpr uint32_t idesc = idesc_bf16_f32(128, NT);
     const uint64_t b_desc0 = smem_desc_sw128(smem_u32(b_ring));
-    uint32_t it = 0, lu = 0;
-    for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-      const Unit un = decode_unit(a, split_k, u);
-      if (!un.ok) continue;
-      const int ab = lu & 1;
-      const uint32_t pab = (lu >> 1) & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&accempty[ab]), pab ^ 1, abort_flag, a.dev_err)))
-        goto mma_done;
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + ab * NT;
-      for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
-        const int nsub = min(KS, un.kb1 - kb);
-        const int sbi = it % S_B;
-        const uint32_t pb = (it / S_B) & 1;
-        const int sa = it % S_A;
-        const uint32_t pa = (it / S_A) & 1;
-        bool ok = mbar_wait(smem_u32(&afull[sa]), pa, abort_flag, a.dev_err);
-        ok = ok && mbar_wait(smem_u32(&bfull[sbi]), pb, abort_flag, a.dev_err);
-        if (!__all_sync(0xffffffffu, ok)) goto mma_done;
-        if (gather) fence_proxy_async_smem();  // cp.async (generic proxy) rows -> tensor core
+    if (elect_one()) {
+      uint32_t it = 0, lu = 0;
+      for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
+        const Unit un = decode_unit(a, split_k, u);
+        if (!un.ok) continue;
+        const int ab = lu & 1;
+        const uint32_t pab = (lu >> 1) & 1;
+        if (!mbar_wait(smem_u32(&accempty[ab]), pab ^ 1, abort_flag, a.dev_err)) goto mma_done;
         tc_fence_after();
-        const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((sbi * Cfg::kBBytes) >> 4);
-        const uint32_t a_tmem = tmem_base + Cfg::kACol0 + sa * (KS * 32);
-        if (elect_one()) {
-          for (int sb = 0; sb < nsub; ++sb) {
-            const uint64_t bd = b_desc + static_cast<uint64_t>((sb * Cfg::kSubB) >> 4);
-            const uint32_t at = a_tmem + sb * 32;
-            mma_ts(d_tmem, at, bd, idesc, (kb > un.kb0 || sb > 0) ? 1u : 0u);
-            mma_ts(d_tmem, at + 8, bd + 2, idesc, 1u);
-            mma_ts(d_tmem, at + 16, bd + 4, idesc, 1u);
-            mma_ts(d_tmem, at + 24, bd + 6, idesc, 1u);
+        const uint32_t d_tmem = tmem_base + ab * NT;
+        for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
+          const int nsub = min(KS, un.kb1 - kb);
+          const int sbi = it % S_B;
+          const uint32_t pb = (it / S_B) & 1;
+          const int sa = it % S_A;
+          const uint32_t pa = (it / S_A) & 1;
+          if (!mbar_wait(smem_u32(&afull[sa]), pa, abort_flag, a.dev_err)) goto mma_done;
+          if (!mbar_wait(smem_u32(&bfull[sbi]), pb, abort_flag, a.dev_err)) goto mma_done;
+          if (gather) fence_proxy_async_smem();  // cp.async (generic proxy) rows -> tensor core
+          tc_fence_after();
+          const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((sbi * Cfg::kBBytes) >> 4);
+          const uint32_t a_tmem = tmem_base + Cfg::kACol0 + sa * (KS * 32);
+          const uint32_t acc0 = kb > un.kb0 ? 1u : 0u;
+          if (nsub == KS) {
+#pragma unroll
+            for (int sb = 0; sb < KS; ++sb) {
+              const uint64_t bd = b_desc + static_cast<uint64_t>((sb * Cfg::kSubB) >> 4);
+              const uint32_t at = a_tmem + sb * 32;
+              mma_ts(d_tmem, at, bd, idesc, sb > 0 ? 1u : acc0);
+              mma_ts(d_tmem, at + 8, bd + 2, idesc, 1u);
+              mma_ts(d_tmem, at + 16, bd + 4, idesc, 1u);
+              mma_ts(d_tmem, at + 24, bd + 6, idesc, 1u);
+            }
+          } else {  // K tail shorter than a full stage
+            for (int sb = 0; sb < nsub; ++sb) {
+              const uint64_t bd = b_desc + static_cast<uint64_t>((sb * Cfg::kSubB) >> 4);
+              const uint32_t at = a_tmem + sb * 32;
+              mma_ts(d_tmem, at, bd, idesc, sb > 0 ? 1u : acc0);
+              mma_ts(d_tmem, at + 8, bd + 2, idesc, 1u);
+              mma_ts(d_tmem, at + 16, bd + 4, idesc, 1u);
+              mma_ts(d_tmem, at + 24, bd + 6, idesc, 1u);
+            }
           }
           mma_commit(smem_u32(&bempty[sbi]));
           mma_commit(smem_u32(&aempty[sa]));
         }
-        __syncwarp();
+        mma_commit(smem_u32(&accfull[ab]));
+        ++lu;
       }
-      if (elect_one()) mma_commit(smem_u32(&accfull[ab]));
-      __syncwarp();
-      ++lu;
-    }
-  mma_done:
-    if (elect_one()) {
+    mma_done:
       mma_commit(smem_u32(drain));
       mbar_wait_plain(smem_u32(drain), 0);
     }
