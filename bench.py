@@ -4,17 +4,21 @@ Workload: Qwen3-30B-A3B-shaped experts (128 experts, top-8, hidden 2048,
 gate_up [128, 1536, 2048], down [128, 2048, 768], uint4 group-32 BF16 scales),
 seeded synthetic inputs, token sweep T in {1, 8, 64, 512, 4096}.
 
-One step = one pass of the whole path for every T of the sweep: align, gate_up
-(activation-row gather, then the GEMM with fused SiLU-and-mul), down, top-k
-weighted sum, each a C-ABI call on the current stream with CUDA events between
-the four stages; the step is captured once as a CUDA graph and replayed.  L2 is flushed (a 512 MB memset,
-outside the events) before every T, so weights and activations come from HBM.
+One step covers every T of the sweep:
+  * per projection, a CUDA graph of R back-to-back calls (gate_up: activation-row
+    gather for large blocks, then the GEMM with fused SiLU-and-mul; down: the
+    GEMM), each call reading its own device copy of the packed weights, with
+    enough copies that at least twice the L2 size of other weight bytes passes
+    between two reads of one copy; per-call time = replay time / R;
+  * the layer path once (align, gate_up, down, top-k weighted sum as separate
+    C-ABI calls, CUDA events between the stages) after a 512 MB L2 flush.
 
 value = weight HBM GB/s over the sweep: sum of the packed weight bytes the two
 projections must read (experts with at least one routed row) divided by the sum
-of the gate_up and down kernel times.  The roofline object describes the GEMM
-kernel (both projections): algorithmic bytes (weights + activations in + outputs)
-per launch over its event-timed duration, against the measured HBM copy peak.
+of the per-call gate_up and down times (medians over the steps).  The roofline
+object describes the GEMM kernel (both projections): algorithmic bytes (weights +
+activations in + outputs) per call over its per-call time, against the measured
+HBM copy peak.
 
 --impl reference times the CPU oracle (single-threaded C++) on a bounded sample
 of the same workload and reports the same metric.
@@ -24,6 +28,7 @@ from __future__ import annotations
 import argparse
 import inspect
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -217,23 +222,83 @@ def run_ours(args, rank, world, local_rank):
             flush.zero_()
             path(c, events[i] if events else None)
 
+    # Back-to-back calls per projection, rotating over device copies of the packed weights so
+    # that every call reads its weights from HBM (>= 2 x L2 of other weight bytes between reuses).
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20))
+
+    def copies_for(touched):
+        return int(min(64, max(2, math.ceil(2 * l2 / max(touched, 1)) + 1)))
+
+    for c in cases:
+        c["n_gu"] = copies_for(c["acct"]["gate_up"]["weight_bytes"])
+        c["n_dn"] = copies_for(c["acct"]["down"]["weight_bytes"])
+        c["R_gu"], c["R_dn"] = max(20, c["n_gu"]), max(20, c["n_dn"])
+    w13s = [w13] + [w13.clone() for _ in range(max(c["n_gu"] for c in cases) - 1)]
+    w2s = [w2] + [w2.clone() for _ in range(max(c["n_dn"] for c in cases) - 1)]
+
+    def align_only(c):
+        lib.load().w4a16_moe_align(
+            lib._ptr(c["ids"]), c["T"], wl.top_k, wl.E, c["block_m"], lib._ptr(c["sorted"]),
+            lib._ptr(c["expert"]), lib._ptr(c["ntp"]), c["cap"], 0, None, lib._stream())
+
+    def gate_up_call(c, W):
+        r = c["routing"]
+        if c["block_m"] >= 64:
+            lib.gather_rows(c["x"], wl.top_k, r, out=c["xs"])
+            lib.moe_gemm(c["xs"], 1, W, r, epilogue=lib.EPILOGUE_SILU_MUL,
+                         row_flags=lib.A_ROWS_SORTED | lib.C_ROWS_SORTED, out=c["h"],
+                         workspace=c["ws"], expected_rows_per_expert=rows_hint[c["T"]])
+        else:
+            lib.moe_gemm(c["x"], wl.top_k, W, r, epilogue=lib.EPILOGUE_SILU_MUL,
+                         row_flags=lib.C_ROWS_SORTED, out=c["h"], workspace=c["ws"],
+                         expected_rows_per_expert=rows_hint[c["T"]])
+
+    def down_call(c, W):
+        lib.moe_gemm(c["h"], 1, W, c["routing"], row_flags=lib.A_ROWS_SORTED | lib.C_FP32,
+                     out=c["y"], workspace=c["ws"], expected_rows_per_expert=rows_hint[c["T"]])
+
+    def back_to_back(c):
+        for i in range(c["R_gu"]):
+            gate_up_call(c, w13s[i % c["n_gu"]])
+        c["ev_bb"][1].record()
+        for i in range(c["R_dn"]):
+            down_call(c, w2s[i % c["n_dn"]])
+
     # Step events: with CUDA-graph capture (events recorded as graph nodes) the device times
     # carry no host launch gaps; without support for that, the step runs eagerly.
     use_graph = "external" in inspect.signature(torch.cuda.Event.__new__).parameters and not args.eager
     mk = (lambda: torch.cuda.Event(enable_timing=True, external=True)) if use_graph else \
          (lambda: torch.cuda.Event(enable_timing=True))
     step_events = [[mk() for _ in range(5)] for _ in cases]
+    for c in cases:
+        c["ev_bb"] = [mk() for _ in range(3)]
 
+    for c in cases:  # routing for the back-to-back calls (static across the calls)
+        align_only(c)
     for _ in range(args.warmup):  # eager warm-up (sets kernel attributes before any capture)
         step()
+        for c in cases:
+            align_only(c)
+            gate_up_call(c, w13)
+            down_call(c, w2)
     torch.cuda.synchronize()
-    graph = None
+    graph, bb_graphs = None, {}
     if use_graph:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             step(step_events)
+        for c in cases:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                c["ev_bb"][0].record()
+                back_to_back(c)
+                c["ev_bb"][2].record()
+            bb_graphs[c["T"]] = g
         for _ in range(args.warmup):
             graph.replay()
+            for c in cases:
+                align_only(c)
+                bb_graphs[c["T"]].replay()
         torch.cuda.synchronize()
 
     # timed region: device time from events, barrier + synchronize on both sides
@@ -244,24 +309,37 @@ def run_ours(args, rank, world, local_rank):
     sampler.start()
     time.sleep(0.3)
     stage_acc = [np.zeros(4) for _ in cases]
+    bb_samples = [([], []) for _ in cases]
     t0 = time.perf_counter()
     for s in range(args.steps):
         if graph is not None:
             graph.replay()
         else:
             step(step_events)
+        for c in cases:
+            flush.zero_()
+            if graph is not None:
+                bb_graphs[c["T"]].replay()
+            else:
+                c["ev_bb"][0].record()
+                back_to_back(c)
+                c["ev_bb"][2].record()
         torch.cuda.synchronize()
-        for i in range(len(cases)):
+        for i, c in enumerate(cases):
             ev = step_events[i]
             stage_acc[i] += [ev[j].elapsed_time(ev[j + 1]) * 1e3 for j in range(4)]
+            eb = c["ev_bb"]
+            bb_samples[i][0].append(eb[0].elapsed_time(eb[1]) * 1e3 / c["R_gu"])
+            bb_samples[i][1].append(eb[1].elapsed_time(eb[2]) * 1e3 / c["R_dn"])
     wall = time.perf_counter() - t0
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
 
-    # per-T stage times (mean over steps, microseconds)
+    # per-T layer stage times (mean over steps) and per-call projection times (median)
     stage_us = [acc / args.steps for acc in stage_acc]
-    step_ms = float(sum(u.sum() for u in stage_us)) / 1e3
+    call_us = [(statistics.median(g), statistics.median(d)) for g, d in bb_samples]
+    step_ms = wall / args.steps * 1e3
 
     # e2e through the public layer call, host buffers, copies inside the timed region
     e2e_events = []
@@ -289,7 +367,7 @@ def run_ours(args, rank, world, local_rank):
 
     # aggregate metric and roofline
     w_bytes = sum(c["acct"]["gate_up"]["weight_bytes"] + c["acct"]["down"]["weight_bytes"] for c in cases)
-    gemm_us = sum(u[1] + u[2] for u in stage_us)
+    gemm_us = sum(g + d for g, d in call_us)
     alg_bytes = sum(c["acct"]["gate_up"]["bytes"] + c["acct"]["down"]["bytes"] for c in cases)
     hbm = float(peaks["hbm_gbs"])
     tflops_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -304,13 +382,16 @@ def run_ours(args, rank, world, local_rank):
     e2e_value = w_bytes * world / (sum(e2e_us) * 1e-6) / 1e9
 
     sweep = []
-    for c, u, e in zip(cases, stage_us, e2e_us):
+    for c, u, cu, e in zip(cases, stage_us, call_us, e2e_us):
         a = c["acct"]
         row = {"T": c["T"], "T_r": a["T_r"], "E_act": a["E_act"], "block_m": c["block_m"],
-               "align_us": round(u[0], 2), "gate_up_us": round(u[1], 2), "down_us": round(u[2], 2),
-               "topk_sum_us": round(u[3], 2), "gate_up_plus_down_us": round(u[1] + u[2], 2),
+               "gate_up_us": round(cu[0], 2), "down_us": round(cu[1], 2),
+               "gate_up_plus_down_us": round(cu[0] + cu[1], 2),
+               "calls_per_graph": [c["R_gu"], c["R_dn"]], "weight_copies": [c["n_gu"], c["n_dn"]],
+               "layer_stage_us": {"align": round(u[0], 2), "gate_up": round(u[1], 2),
+                                  "down": round(u[2], 2), "topk_sum": round(u[3], 2)},
                "layer_e2e_us": round(e, 2)}
-        for name, t_us in (("gate_up", u[1]), ("down", u[2])):
+        for name, t_us in (("gate_up", cu[0]), ("down", cu[1])):
             d = a[name]
             roof_us = max(d["bytes"] / (hbm * 1e9), d["flops"] / (tflops_peak * 1e12)) * 1e6
             row[f"{name}_weight_GBps"] = round(d["weight_bytes"] / (t_us * 1e-6) / 1e9, 1)
@@ -337,10 +418,14 @@ def run_ours(args, rank, world, local_rank):
                         f"gate_up [{wl.E},{2 * wl.I},{wl.H}], down [{wl.E},{wl.H},{wl.I}], "
                         f"uint4 group-32 BF16 scales",
             "tokens": tokens,
-            "l2": "flushed by a 512 MB memset before every T (outside the timed events)",
-            "timing": ("CUDA graph of the step replayed K times; CUDA events recorded as graph "
+            "l2": ("per-call times: inputs larger than L2 in effect (each call reads one of "
+                   "n device copies of the packed weights, >= 2 x L2 of other weight bytes "
+                   "between reuses); layer stages: 512 MB memset flush before every T"),
+            "timing": ("per-call = CUDA events around a CUDA graph of R back-to-back calls / R, "
+                       "median over the K steps; layer stages: CUDA events recorded as graph "
                        "nodes around every kernel" if use_graph else
-                       "eager launches; CUDA events around every kernel"),
+                       "eager launches; CUDA events around R back-to-back calls and around "
+                       "every layer stage"),
             "parallelism": "replicas" if world > 1 else "single GPU",
             "sweep": sweep,
         },
@@ -356,7 +441,9 @@ def run_ours(args, rank, world, local_rank):
         },
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": sum(5 if c["block_m"] >= 64 else 4 for c in cases) * args.steps,
+        "gpu_launches": (sum(5 if c["block_m"] >= 64 else 4 for c in cases)
+                         + sum(1 + c["R_gu"] * (2 if c["block_m"] >= 64 else 1) + c["R_dn"]
+                               for c in cases)) * args.steps,
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -218,6 +218,14 @@ class PackedWeights:
     def nbytes(self) -> int:
         return int(self.desc.bytes)
 
+    def clone(self) -> "PackedWeights":
+        """A second device copy of the same packed weights (a device-to-device copy of the blob)."""
+        blob = self.blob.clone()
+        desc = PackedDesc()
+        ctypes.memmove(ctypes.byref(desc), ctypes.byref(self.desc), ctypes.sizeof(PackedDesc))
+        desc.data = blob.data_ptr()
+        return PackedWeights(blob, desc)
+
 
 def packed_bytes(E: int, N: int, K: int, paired: bool = False) -> int:
     return int(load().w4a16_packed_bytes(E, N, K, 32, PACK_GATE_UP_PAIRED if paired else 0))
