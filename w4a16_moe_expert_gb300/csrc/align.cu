@@ -5,16 +5,23 @@
 // num_tokens_padded from an over-allocated align step, read on the device only, so the
 // whole path stays CUDA-graph capturable.
 //
-// One CTA of 1024 threads.  Each of the 32 warps owns a contiguous range of slots, which
-// keeps the sort stable without a global sort: a warp counts its range per expert, the
-// per-expert counts are scanned over warps and experts, and each warp then places its slots
-// in order (a warp-wide match gives each slot its rank among equal ids).
+// One thread-block cluster of up to 8 CTAs x 1024 threads.  The slots are cut into contiguous
+// chunks, one per CTA, and each CTA's chunk into contiguous ranges, one per warp, which keeps
+// the sort stable without a global sort: every warp counts its range per expert, the CTAs
+// exchange their per-expert totals through distributed shared memory, the counts are scanned
+// over CTAs, warps and experts, and each warp then places its slots in order (a warp-wide
+// match gives each slot its rank among equal ids).
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 
 namespace w4a16 {
 
+namespace cg = cooperative_groups;
+
 constexpr int kAlignThreads = 1024;
 constexpr int kAlignWarps = kAlignThreads / 32;
+constexpr int kAlignMaxCluster = 8;
 
 __global__ void __launch_bounds__(kAlignThreads, 1)
     moe_align_kernel(const int32_t* __restrict__ topk_ids, int n_slots, int E, int block_m,
@@ -23,26 +30,34 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
                      int32_t* dev_err, int32_t* zero_words, int n_zero_words) {
   extern __shared__ int32_t sm[];
   int32_t* cnt = sm;                      // [32][E]: per-warp counts, later per-warp cursors
-  int32_t* start = sm + kAlignWarps * E;  // [E + 1]: padded exclusive prefix
+  int32_t* start = cnt + kAlignWarps * E;  // [E + 1]: padded exclusive prefix
+  int32_t* cta_cnt = start + E + 1;        // [E]: this CTA's count per expert (read by peers)
+  int32_t* tot = cta_cnt + E;              // [E]: count per expert over all CTAs
+  int32_t* pre = tot + E;                  // [E]: count per expert in the chunks before ours
   __shared__ int32_t warp_sums[kAlignWarps];
   __shared__ int bad_id;
 
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int ncta = static_cast<int>(cluster.num_blocks());
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gtid = rank * kAlignThreads + tid, gthreads = ncta * kAlignThreads;
   const int32_t sentinel = n_slots;
   pdl_launch_dependents();  // the next kernel may start its prologue; it waits for our results
   pdl_wait();               // topk_ids may come from the previous kernel in the stream
 
   for (int i = tid; i < kAlignWarps * E; i += kAlignThreads) cnt[i] = 0;
   if (tid == 0) bad_id = 0;
-  for (int i = tid; i < n_zero_words; i += kAlignThreads) zero_words[i] = 0;
-  // all rows start as sentinels; real slots overwrite them after the barriers below
-  for (int64_t p = tid; p < capacity; p += kAlignThreads) sorted_ids[p] = sentinel;
+  for (int i = gtid; i < n_zero_words; i += gthreads) zero_words[i] = 0;
   __syncthreads();
 
-  // ---- count per (warp, expert) ----
-  const int per_warp = ((n_slots + kAlignWarps - 1) / kAlignWarps + 31) & ~31;
-  const int lo = warp * per_warp;
-  const int hi = min(n_slots, lo + per_warp);
+  // ---- count per (warp, expert) over this CTA's chunk ----
+  const int per_cta = ((n_slots + ncta - 1) / ncta + 1023) & ~1023;
+  const int c_lo = min(n_slots, rank * per_cta);
+  const int c_hi = min(n_slots, c_lo + per_cta);
+  const int per_warp = per_cta / kAlignWarps;  // a multiple of 32
+  const int lo = min(c_hi, c_lo + warp * per_warp);
+  const int hi = min(c_hi, lo + per_warp);
   for (int base = lo; base < hi; base += 32) {
     const int i = base + lane;
     int e = (i < hi) ? topk_ids[i] : -1;
@@ -55,7 +70,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
   }
   __syncthreads();
 
-  // ---- per expert: totals, warp offsets inside the expert, padded size ----
+  // ---- per expert: warp offsets inside the CTA, the CTA's count ----
   for (int e = tid; e < E; e += kAlignThreads) {
     int run = 0;
     for (int w = 0; w < kAlignWarps; ++w) {
@@ -63,7 +78,24 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
       cnt[w * E + e] = run;
       run += c;
     }
-    start[e] = (run + block_m - 1) / block_m * block_m;  // padded size for now
+    cta_cnt[e] = run;
+  }
+  if (ncta > 1) cluster.sync(); else __syncthreads();  // every CTA's counts are visible
+
+  // ---- per expert: total, count before this chunk, padded size ----
+  for (int e = tid; e < E; e += kAlignThreads) {
+    int all = cta_cnt[e], before = 0;
+    if (ncta > 1) {
+      all = 0;
+      for (int r = 0; r < ncta; ++r) {
+        const int c = *cluster.map_shared_rank(cta_cnt + e, r);
+        all += c;
+        if (r < rank) before += c;
+      }
+    }
+    tot[e] = all;
+    pre[e] = before;
+    start[e] = (all + block_m - 1) / block_m * block_m;  // padded size for now
   }
   __syncthreads();
 
@@ -95,10 +127,10 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
   const int ntp = start[E];
 
   // ---- per-warp cursors become absolute positions ----
-  for (int i = tid; i < kAlignWarps * E; i += kAlignThreads) cnt[i] += start[i % E];
-  // ---- expert of every block ----
+  for (int i = tid; i < kAlignWarps * E; i += kAlignThreads) cnt[i] += start[i % E] + pre[i % E];
+  // ---- expert of every block (spread over the cluster) ----
   const int64_t nblocks = capacity / block_m;
-  for (int64_t b = tid; b < nblocks; b += kAlignThreads) {
+  for (int64_t b = gtid; b < nblocks; b += gthreads) {
     const int64_t row = b * block_m;
     int owner = -1;
     if (row < ntp) {  // last expert whose start is <= row (experts with no rows have size 0)
@@ -111,6 +143,13 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
     }
     expert_ids[b] = owner;
   }
+  // ---- sentinels: the padding rows of every expert, and everything from num_tokens_padded on ----
+  for (int e = gtid; e < E; e += gthreads) {
+    const int end = start[e + 1];  // start[E] is num_tokens_padded
+    for (int p = start[e] + tot[e]; p < end; ++p)
+      if (p < capacity) sorted_ids[p] = sentinel;
+  }
+  for (int64_t p = static_cast<int64_t>(ntp) + gtid; p < capacity; p += gthreads) sorted_ids[p] = sentinel;
   __syncthreads();
 
   // ---- stable placement ----
@@ -121,8 +160,8 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
     if (e < -1 || e >= E) e = -1;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     if (e >= 0) {
-      const int rank = __popc(peers & ((1u << lane) - 1u));
-      const int pos = cnt[warp * E + e] + rank;
+      const int r = __popc(peers & ((1u << lane) - 1u));
+      const int pos = cnt[warp * E + e] + r;
       if (pos < capacity) sorted_ids[pos] = i; else overflow = true;
     }
     __syncwarp();
@@ -130,12 +169,13 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
     __syncwarp();
   }
   if (overflow) set_dev_err(dev_err, W4A16_DEVERR_CAPACITY);
-  if (tid == 0) {
+  if (rank == 0 && tid == 0) {
     *ntp_out = (ntp <= capacity) ? ntp : static_cast<int32_t>(capacity / block_m * block_m);
     if (ntp > capacity) set_dev_err(dev_err, W4A16_DEVERR_CAPACITY);
   }
   __syncthreads();
   if (tid == 0 && bad_id) set_dev_err(dev_err, W4A16_DEVERR_BAD_EXPERT_ID);
+  if (ncta > 1) cluster.sync();  // peers may still be reading this CTA's counts
 }
 
 // Activation rows in aligned order: out[p, :] = x[sorted_ids[p] / a_row_div, :] for every
@@ -190,7 +230,15 @@ cudaError_t launch_gather_rows(const uint16_t* x, int64_t ldx, int K, int a_row_
 }
 
 size_t align_smem_bytes(int E) {
-  return static_cast<size_t>(kAlignWarps * E + E + 1) * sizeof(int32_t);
+  return static_cast<size_t>(kAlignWarps * E + 4 * E + 1) * sizeof(int32_t);
+}
+
+// Cluster size for n_slots slots: one CTA while each warp's range is at most two passes of 32,
+// doubling up to eight CTAs for prefill-sized routings.
+static int align_cluster_size(int n_slots) {
+  int c = 1;
+  while (c < kAlignMaxCluster && n_slots > c * 2 * kAlignThreads) c *= 2;
+  return c;
 }
 
 cudaError_t launch_moe_align(const int32_t* topk_ids, int n_slots, int E, int block_m,
@@ -202,16 +250,21 @@ cudaError_t launch_moe_align(const int32_t* topk_ids, int n_slots, int E, int bl
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
+  const int cluster = align_cluster_size(n_slots);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(1);
+  cfg.gridDim = dim3(cluster);
   cfg.blockDim = dim3(kAlignThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;  // one CTA launches as a plain grid
+  attr[1].val.clusterDim.x = cluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = cluster > 1 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, moe_align_kernel, topk_ids, n_slots, E, block_m, sorted_ids,
                             expert_ids, ntp, capacity, validate, dev_err, zero_words,
                             n_zero_words);

@@ -576,11 +576,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // Host side: planner, tensor maps and launcher.
 // ------------------------------------------------------------------------------------------
 
-// Stage depth: the MMA warp pays a fixed cost of a few hundred cycles per burst of MMAs on top
-// of ~13 cycles per MMA, so the small-N (weight-bound) blocks issue 16 MMAs per stage (four
-// 64-wide K blocks, 18432-byte weight copies); larger blocks keep two (TMEM and activation
-// tiles then bound the stage size).
-template <int NT> struct StageK { static constexpr int value = NT <= 32 ? 4 : 2; };
+// Stage depth: every stage costs barrier round trips and an MMA burst on top of its bytes, so
+// blocks up to 64 tokens move four 64-wide K blocks per stage (18432-byte weight copies, 16
+// MMAs; measured fastest on GB300 against 2, 3, 5 and 6); 128-token blocks keep two, since
+// their activation tiles and accumulators then bound shared memory and TMEM.
+template <int NT> struct StageK { static constexpr int value = NT <= 64 ? 4 : 2; };
 
 int stages_for_block_m(int block_m) {
   switch (block_m) {
