@@ -186,6 +186,45 @@ w4a16_status_t w4a16_gather_rows(const uint16_t* x, int64_t ldx, int K, int a_ro
                                  w4a16_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Grouped contracts ("Grouped SM90 kernels": contiguous prefill and masked decode).  The page
+ * builds these as a second kernel family with its own weight packers; here a small layout
+ * kernel turns each layout into the aligned routing above and the indexed GEMM computes, so a
+ * weight packed once by w4a16_pack_weights serves every contract (the gate/up pairing it
+ * records is still checked: SiLU-and-mul needs a W4A16_PACK_GATE_UP_PAIRED weight).  Output
+ * widths, alignment rules for A and C and the epilogues are those of w4a16_moe_gemm.
+ *
+ * Contiguous: A device BF16 [m, K] (row stride lda), rows concatenated by expert with each
+ *   expert's group padded to a 128-row boundary (m % 128 == 0); m_indices device int32 [m],
+ *   the expert of each row or -1 for padding.
+ *     C[r, :] = A[r, :] . dequant(W[m_indices[r]])^T            for m_indices[r] >= 0.
+ *   Padding rows of a 128-row block that holds valid rows are written as zeros; a block of
+ *   padding only is left untouched.  A block whose valid ids differ, or an id outside [-1, E),
+ *   sets W4A16_DEVERR_BAD_EXPERT_ID in *dev_err (when given); such a block is computed with
+ *   the expert of its first valid row and out-of-range ids count as padding.
+ * Masked: A device BF16 [G * max_m, K] (a [G, max_m, K] tensor is the same memory); masked_m
+ *   device int32 [G], the valid rows of each expert (clamped to [0, max_m]; a value outside
+ *   sets W4A16_DEVERR_CAPACITY); expected_m > 0 a host hint of rows per expert that selects
+ *   the block size only; G must equal the weight's E (G <= 1024).
+ *     C[g * max_m + r, :] = A[g * max_m + r, :] . dequant(W[g])^T  for r < masked_m[g];
+ *   the other rows of C are left untouched (consumers ignore them).
+ * workspace: device scratch of the matching *_workspace_size() bytes (it holds the routing),
+ *   256-byte aligned, no initial contents required; concurrent calls must not share it.
+ * Both are stream-ordered with no host synchronisation (graph capturable).
+ * ---------------------------------------------------------------------------------------- */
+size_t w4a16_contiguous_workspace_size(int64_t m);
+w4a16_status_t w4a16_contiguous_gemm(const uint16_t* A, int64_t lda, int64_t m,
+                                     const int32_t* m_indices, const w4a16_packed_weights_t* W,
+                                     int epilogue, uint16_t* C, int64_t ldc, void* workspace,
+                                     size_t workspace_bytes, int32_t* dev_err,
+                                     w4a16_stream_t stream);
+size_t w4a16_masked_workspace_size(int G, int max_m, int expected_m);
+w4a16_status_t w4a16_masked_gemm(const uint16_t* A, int64_t lda, int G, int max_m,
+                                 const int32_t* masked_m, int expected_m,
+                                 const w4a16_packed_weights_t* W, int epilogue, uint16_t* C,
+                                 int64_t ldc, void* workspace, size_t workspace_bytes,
+                                 int32_t* dev_err, w4a16_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * Indexed GEMM that allocates nothing.  The paper has no counterpart: this entry point exists
  * for callers that cannot hand the library a workspace, such as an inference-engine plugin
  * whose enqueue hook receives only its input and output buffers, or a serving loop that must

@@ -60,6 +60,8 @@ def lib():
                 "w4a16_oracle_gemm_rows": (None, [vp, i32, i32, vp, vp, i32, i32, vp, vp, i64, vp]),
                 "w4a16_oracle_moe_gemm": (i32, [vp, i32, i32, vp, vp, i32, i32, vp, vp, i32, i32,
                                                 i32, i32, i32, vp, vp]),
+                "w4a16_oracle_contiguous_gemm": (i32, [vp, i64, i32, vp, vp, i32, i32, i32, vp, vp]),
+                "w4a16_oracle_masked_gemm": (i32, [vp, i32, i32, i32, vp, vp, i32, i32, vp, vp]),
                 "w4a16_oracle_silu_mul": (None, [vp, i64, i32, vp]),
                 "w4a16_oracle_topk_sum": (None, [vp, vp, vp, i32, i32, i32, vp]),
                 "w4a16_oracle_moe_layer": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
@@ -195,6 +197,40 @@ def moe_gemm(A, a_row_div: int, qweight, scales, sorted_ids, expert_ids, ntp: in
         with ThreadPoolExecutor(len(bounds) - 1) as ex:
             list(ex.map(lambda lh: run(*lh), zip(bounds[:-1], bounds[1:])))
     return torch.from_numpy(C) if out_f32 else _bf16_tensor(C)
+
+
+def contiguous_gemm(A, qweight, scales, m_indices, group: int = 32) -> torch.Tensor:
+    """Contiguous grouped layout: C[r] = A[r] @ dequant(W[m_indices[r]]).T, padding rows 0."""
+    a = _np(A, np.uint16)
+    q = _np(qweight, np.int32)
+    s = _np(scales, np.uint16)
+    mi = _np(m_indices, np.int32)
+    m, K = a.shape
+    E, N = q.shape[0], q.shape[1]
+    C = np.zeros((m, N), np.uint16)
+    rc = lib().w4a16_oracle_contiguous_gemm(_ptr(a), m, K, _ptr(q), _ptr(s), E, N, group,
+                                            _ptr(mi), _ptr(C))
+    if rc:
+        raise ValueError(f"oracle contiguous_gemm failed with code {rc}")
+    return _bf16_tensor(C)
+
+
+def masked_gemm(A, qweight, scales, masked_m, max_m: int, group: int = 32) -> torch.Tensor:
+    """Masked grouped layout over A [G * max_m, K]: rows g*max_m + r, r < masked_m[g], of the
+    flat [G * max_m, N] output; the other rows are returned as 0 (undefined by the contract)."""
+    a = _np(A, np.uint16).reshape(-1, _np(A, np.uint16).shape[-1])
+    q = _np(qweight, np.int32)
+    s = _np(scales, np.uint16)
+    mm = _np(masked_m, np.int32)
+    G = q.shape[0]
+    N = q.shape[1]
+    K = a.shape[-1]
+    C = np.zeros((G * max_m, N), np.uint16)
+    rc = lib().w4a16_oracle_masked_gemm(_ptr(a), G, max_m, K, _ptr(q), _ptr(s), N, group,
+                                        _ptr(mm), _ptr(C))
+    if rc:
+        raise ValueError(f"oracle masked_gemm failed with code {rc}")
+    return _bf16_tensor(C)
 
 
 def silu_mul(C) -> torch.Tensor:

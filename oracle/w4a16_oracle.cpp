@@ -259,6 +259,44 @@ void w4a16_oracle_topk_sum(const float* Y, const int32_t* topk_ids, const float*
   }
 }
 
+// ---- grouped contracts -------------------------------------------------------------
+// "Grouped SM90 kernels" (vLLM x Novita AI: Chord): the contiguous prefill layout has its rows
+// concatenated by expert, each group padded to a 128-row boundary, with m_indices[r] the
+// expert of row r or -1 for padding; the output row r is A[r] times the dequantised weight of
+// that expert.  Padding rows are zero here.
+int w4a16_oracle_contiguous_gemm(const uint16_t* A, int64_t m, int K, const int32_t* qweight,
+                                 const uint16_t* scales, int E, int N, int group,
+                                 const int32_t* m_indices, uint16_t* C) {
+  if (K % 8 || K % group || m % 128) return -3;
+  for (int64_t r = 0; r < m; ++r) {
+    const int32_t e = m_indices[r];
+    uint16_t* out = C + r * N;
+    if (e < 0 || e >= E) {
+      for (int n = 0; n < N; ++n) out[n] = 0;
+      continue;
+    }
+    gemm_one_row(A + r * K, K, qweight, scales, N, group, e, out, nullptr);
+  }
+  return 0;
+}
+
+// Same page, masked decode layout: a fixed budget of max_m rows per expert g (rows
+// g * max_m .. g * max_m + max_m - 1 of A and of the flat output), of which the first
+// masked_m[g] are valid; only those output rows are defined (the others are left as they are).
+int w4a16_oracle_masked_gemm(const uint16_t* A, int G, int max_m, int K, const int32_t* qweight,
+                             const uint16_t* scales, int N, int group, const int32_t* masked_m,
+                             uint16_t* C) {
+  if (K % 8 || K % group || max_m <= 0) return -3;
+  for (int g = 0; g < G; ++g) {
+    const int valid = masked_m[g] < 0 ? 0 : (masked_m[g] > max_m ? max_m : masked_m[g]);
+    for (int r = 0; r < valid; ++r) {
+      const int64_t row = static_cast<int64_t>(g) * max_m + r;
+      gemm_one_row(A + row * K, K, qweight, scales, N, group, g, C + row * N, nullptr);
+    }
+  }
+  return 0;
+}
+
 // ---- whole layer -----------------------------------------------------------------
 
 int w4a16_oracle_moe_layer(const uint16_t* x, const int32_t* w13_q, const uint16_t* w13_s,

@@ -471,3 +471,77 @@ def test_layer_dropped_slots_give_zero_rows():
     out = oracle.moe_layer(inp.x, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s, ids, inp.topk_weights)
     assert torch.all(out[3].float() == 0)
     assert torch.any(out[2].float() != 0)
+
+
+# ---- grouped contracts ("Grouped SM90 kernels": contiguous prefill, masked decode) ----------
+
+def _contiguous_problem(seed, groups=((0, 100), (2, 128), (1, 3)), E=3, N=32, K=64):
+    """Rows concatenated by expert, each group padded to a 128-row boundary with -1."""
+    qw, sc = workloads.draw_weights(E, N, K, seed=seed)
+    ids = []
+    for e, rows in groups:
+        pad = (-rows) % 128
+        ids += [e] * rows + [-1] * pad
+    m_indices = torch.tensor(ids, dtype=torch.int32)
+    x = workloads.draw_activations(len(ids), K, seed=seed)
+    return qw, sc, x, m_indices
+
+
+def test_contiguous_brute_force_rows_and_zero_padding():
+    qw, sc, x, mi = _contiguous_problem(21)
+    C = bf16_np(oracle.contiguous_gemm(x, qw, sc, mi))
+    wd = dequant_np(qw.numpy(), sc.view(torch.int16).numpy())
+    xa = bf16_np(x)
+    for r in range(mi.numel()):
+        e = int(mi[r])
+        if e < 0:
+            assert np.all(C[r] == 0)
+            continue
+        ref = wd[e] @ xa[r]  # float64 sum of exact products
+        assert np.all(np.abs(C[r] - ref) <= ulp_bf16(ref) + 1e-12)
+
+
+def test_contiguous_single_expert_equals_torch_matmul():
+    qw, sc = workloads.draw_weights(2, 64, 128, seed=22)
+    x = workloads.draw_activations(256, 128, seed=22)
+    mi = torch.ones(256, dtype=torch.int32)
+    C = oracle.contiguous_gemm(x, qw, sc, mi).float()
+    ref = torch.matmul(x.float(), oracle.dequant(qw, sc)[1].float().T)
+    assert torch.all((C - ref).abs() <= torch.from_numpy(ulp_bf16(ref.numpy())).float() + 1e-6)
+
+
+def test_contiguous_group_order_permutes_rows():
+    qw, sc, x, mi = _contiguous_problem(23, groups=((0, 128), (1, 128)), E=2)
+    C = oracle.contiguous_gemm(x, qw, sc, mi)
+    swapped_x = torch.cat([x[128:], x[:128]])
+    swapped_mi = torch.cat([mi[128:], mi[:128]])
+    D = oracle.contiguous_gemm(swapped_x, qw, sc, swapped_mi)
+    assert np.array_equal(bits(D), bits(torch.cat([C[128:], C[:128]])))
+
+
+def test_masked_valid_rows_equal_per_expert_matmul_and_rest_untouched():
+    G, N, K, max_m = 3, 32, 64, 16
+    qw, sc = workloads.draw_weights(G, N, K, seed=24)
+    x = workloads.draw_activations(G * max_m, K, seed=24)
+    mm = torch.tensor([5, 0, 16], dtype=torch.int32)
+    C = oracle.masked_gemm(x, qw, sc, mm, max_m).float()
+    wd = oracle.dequant(qw, sc)
+    for g in range(G):
+        rows = slice(g * max_m, g * max_m + int(mm[g]))
+        ref = torch.matmul(x[rows].float(), wd[g].float().T)
+        assert torch.all((C[rows] - ref).abs() <= torch.from_numpy(ulp_bf16(ref.numpy())).float() + 1e-6)
+        assert torch.all(C[g * max_m + int(mm[g]):(g + 1) * max_m] == 0)
+
+
+def test_masked_equals_contiguous_on_the_same_rows():
+    # Masked rows laid out as a contiguous problem (budget = 128 rows per expert) give the
+    # same bits: both are per-row products with that row's expert.
+    G, N, K, max_m = 2, 32, 64, 128
+    qw, sc = workloads.draw_weights(G, N, K, seed=25)
+    x = workloads.draw_activations(G * max_m, K, seed=25)
+    mm = torch.tensor([100, 7], dtype=torch.int32)
+    M = oracle.masked_gemm(x, qw, sc, mm, max_m)
+    mi = torch.tensor([0] * 100 + [-1] * 28 + [1] * 7 + [-1] * 121, dtype=torch.int32)
+    Cc = oracle.contiguous_gemm(x, qw, sc, mi)
+    valid = mi >= 0
+    assert np.array_equal(bits(M[valid]), bits(Cc[valid]))

@@ -23,7 +23,7 @@ from . import build as _build
 
 __all__ = [
     "load", "library_path", "align_capacity", "moe_align", "PackedWeights", "pack_weights",
-    "Routing", "moe_gemm", "gather_rows", "topk_sum", "moe_layer", "layer_workspace_size", "plan_block_m",
+    "Routing", "moe_gemm", "gather_rows", "contiguous_gemm", "masked_gemm", "topk_sum", "moe_layer", "layer_workspace_size", "plan_block_m",
     "plan_gemm", "debug_dequant", "gemm_workspace_size", "EPILOGUE_NONE", "EPILOGUE_SILU_MUL",
     "A_ROWS_SORTED", "C_ROWS_SORTED", "C_FP32", "PACK_GATE_UP_PAIRED", "LibraryError",
 ]
@@ -93,6 +93,12 @@ _SIGNATURES = {
     "w4a16_gather_rows": (_I32, [_VP, _I64, _I32, _I32, _P(RoutingDesc), _VP, _I64, _VP]),
     "w4a16_moe_gemm_static_scratch": (_I32, [_VP, _I64, _I32, _P(PackedDesc), _P(RoutingDesc), _I32,
                                              _U32, _VP, _I64, _I32, _P(ScheduleDesc), _VP, _VP]),
+    "w4a16_contiguous_workspace_size": (_SZ, [_I64]),
+    "w4a16_contiguous_gemm": (_I32, [_VP, _I64, _I64, _VP, _P(PackedDesc), _I32, _VP, _I64, _VP, _SZ,
+                                     _VP, _VP]),
+    "w4a16_masked_workspace_size": (_SZ, [_I32, _I32, _I32]),
+    "w4a16_masked_gemm": (_I32, [_VP, _I64, _I32, _I32, _VP, _I32, _P(PackedDesc), _I32, _VP, _I64,
+                                 _VP, _SZ, _VP, _VP]),
     "w4a16_plan_block_m": (_I32, [_I32, _I32, _I32, _I32]),
     "w4a16_layer_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32, _I32]),
     "w4a16_moe_layer": (_I32, [_VP, _P(PackedDesc), _P(PackedDesc), _VP, _VP, _I32, _I32, _I32, _I32,
@@ -328,6 +334,53 @@ def moe_gemm_static_scratch(A: torch.Tensor, a_row_div: int, W: PackedWeights, r
     _check("w4a16_moe_gemm_static_scratch", load().w4a16_moe_gemm_static_scratch(
         _ptr(A), A.stride(0), a_row_div, ctypes.byref(W.desc), ctypes.byref(rd), epilogue, row_flags,
         _ptr(out), out.stride(0), expected_rows_per_expert, ctypes.byref(sched), _ptr(dev_err),
+        _stream()))
+    return out
+
+
+def contiguous_gemm(A: torch.Tensor, W: PackedWeights, m_indices: torch.Tensor,
+                    epilogue: int = EPILOGUE_NONE, out: Optional[torch.Tensor] = None,
+                    workspace: Optional[torch.Tensor] = None,
+                    dev_err: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Contiguous grouped layout: A [m, K] rows concatenated by expert (groups padded to 128
+    rows), m_indices int32 [m] (-1 for padding) -> C [m, N or N/2]."""
+    _cuda(A, torch.bfloat16, "A")
+    _cuda(m_indices, torch.int32, "m_indices")
+    m = A.shape[0]
+    width = W.N // 2 if epilogue == EPILOGUE_SILU_MUL else W.N
+    if out is None:
+        out = torch.empty((m, width), dtype=torch.bfloat16, device=A.device)
+    _cuda(out, torch.bfloat16, "out")
+    need = int(load().w4a16_contiguous_workspace_size(m))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=A.device)
+    _check("w4a16_contiguous_gemm", load().w4a16_contiguous_gemm(
+        _ptr(A), A.stride(0), m, _ptr(m_indices), ctypes.byref(W.desc), epilogue, _ptr(out),
+        out.stride(0), _ptr(workspace), workspace.numel(), _ptr(dev_err), _stream()))
+    return out
+
+
+def masked_gemm(A: torch.Tensor, W: PackedWeights, masked_m: torch.Tensor, expected_m: int,
+                epilogue: int = EPILOGUE_NONE, out: Optional[torch.Tensor] = None,
+                workspace: Optional[torch.Tensor] = None,
+                dev_err: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Masked grouped layout: A [G, max_m, K] or [G * max_m, K], masked_m int32 [G] valid rows
+    -> flat C [G * max_m, N or N/2] (rows past each expert's count are left as they are)."""
+    _cuda(A, torch.bfloat16, "A")
+    _cuda(masked_m, torch.int32, "masked_m")
+    G = masked_m.numel()
+    A2 = A.reshape(-1, A.shape[-1])
+    max_m = A2.shape[0] // max(G, 1)
+    width = W.N // 2 if epilogue == EPILOGUE_SILU_MUL else W.N
+    if out is None:
+        out = torch.zeros((G * max_m, width), dtype=torch.bfloat16, device=A.device)
+    _cuda(out, torch.bfloat16, "out")
+    need = int(load().w4a16_masked_workspace_size(G, max_m, expected_m))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=A.device)
+    _check("w4a16_masked_gemm", load().w4a16_masked_gemm(
+        _ptr(A2), A2.stride(0), G, max_m, _ptr(masked_m), expected_m, ctypes.byref(W.desc),
+        epilogue, _ptr(out), out.stride(0), _ptr(workspace), workspace.numel(), _ptr(dev_err),
         _stream()))
     return out
 

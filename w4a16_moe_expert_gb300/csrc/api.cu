@@ -21,6 +21,12 @@ cudaError_t launch_gather_rows(const uint16_t* x, int64_t ldx, int K, int a_row_
                                const int32_t* sorted_ids, const int32_t* ntp, int total_slots,
                                int64_t capacity, uint16_t* out, int64_t ldo, int num_sms,
                                cudaStream_t stream);
+cudaError_t launch_contiguous_layout(const int32_t* m_indices, int m, int E, int32_t* sorted_ids,
+                                     int32_t* expert_ids, int32_t* ntp, int32_t* dev_err,
+                                     int num_sms, cudaStream_t stream);
+cudaError_t launch_masked_layout(const int32_t* masked_m, int G, int max_m, int block_m,
+                                 int64_t capacity, int32_t* sorted_ids, int32_t* expert_ids,
+                                 int32_t* ntp, int32_t* dev_err, cudaStream_t stream);
 cudaError_t launch_pack(const int32_t* qweight, const uint16_t* scales, int E, int N, int K,
                         uint32_t flags, void* packed, cudaStream_t stream);
 cudaError_t launch_debug_dequant(const void* packed, int e, int N, int K, uint32_t flags,
@@ -372,6 +378,112 @@ w4a16_status_t w4a16_moe_gemm(const uint16_t* A, int64_t lda, int a_row_div,
     return fail(W4A16_INVALID_ARG, "unknown row flags");
   GemmCall c{A, lda, a_row_div, W, routing, epilogue, row_flags, C, ldc, workspace,
              workspace_bytes, expected_rows_per_expert, schedule, dev_err, 0};
+  return run_gemm(c, dev, stream);
+}
+
+// ---- grouped contracts: a layout kernel builds the routing, the indexed GEMM computes ----
+
+struct GroupedLayout {  // routing arrays inside the caller's workspace
+  size_t off_expert, off_ntp, total;
+};
+
+static GroupedLayout grouped_layout(int64_t capacity, int block_m) {
+  GroupedLayout L;
+  L.off_expert = round_up(static_cast<size_t>(capacity) * 4, 256);
+  L.off_ntp = L.off_expert + round_up(static_cast<size_t>(capacity / block_m) * 4, 256);
+  L.total = L.off_ntp + 256;
+  return L;
+}
+
+size_t w4a16_contiguous_workspace_size(int64_t m) {
+  if (m <= 0 || m % 128 || m >= (int64_t(1) << 31)) return 0;
+  return grouped_layout(m, 128).total;
+}
+
+w4a16_status_t w4a16_contiguous_gemm(const uint16_t* A, int64_t lda, int64_t m,
+                                     const int32_t* m_indices, const w4a16_packed_weights_t* W,
+                                     int epilogue, uint16_t* C, int64_t ldc, void* workspace,
+                                     size_t workspace_bytes, int32_t* dev_err,
+                                     w4a16_stream_t stream) {
+  w4a16_status_t st = check_packed(W);
+  if (st != W4A16_OK) return st;
+  if (m < 0 || m % 128 || m >= (int64_t(1) << 31))
+    return fail(W4A16_INVALID_ARG, "m must be a multiple of 128 below 2^31");
+  if (m == 0) return W4A16_OK;
+  if (!m_indices || !workspace || reinterpret_cast<uintptr_t>(workspace) % 256)
+    return fail(W4A16_INVALID_ARG, "m_indices and a 256-byte aligned workspace are required");
+  const GroupedLayout L = grouped_layout(m, 128);
+  if (workspace_bytes < L.total)
+    return fail(W4A16_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes", L.total);
+  DeviceFacts dev;
+  st = device_facts(&dev);
+  if (st != W4A16_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* sorted_ids = reinterpret_cast<int32_t*>(ws);
+  int32_t* expert_ids = reinterpret_cast<int32_t*>(ws + L.off_expert);
+  int32_t* ntp = reinterpret_cast<int32_t*>(ws + L.off_ntp);
+  cudaError_t err = launch_contiguous_layout(m_indices, static_cast<int>(m), W->E, sorted_ids,
+                                             expert_ids, ntp, dev_err, dev.num_sms, stream);
+  if (err != cudaSuccess) return cuda_fail(err, "contiguous layout launch");
+  const w4a16_routing_t R{sorted_ids, expert_ids, ntp, m, 128, static_cast<int32_t>(m)};
+  const w4a16_schedule_t one_split{1, 0};
+  GemmCall c{A, lda, 1, W, &R, epilogue, W4A16_A_ROWS_SORTED | W4A16_C_ROWS_SORTED, C, ldc,
+             nullptr, 0, 128, &one_split, dev_err, 0};
+  return run_gemm(c, dev, stream);
+}
+
+// Block size of the masked layout from the expected rows per expert (the indexed planner's
+// thresholds).
+static int masked_block_m(int expected_m) {
+  if (expected_m <= 12) return 16;
+  if (expected_m <= 24) return 32;
+  if (expected_m <= 48) return 64;
+  return 128;
+}
+
+static int64_t masked_capacity(int G, int max_m, int block_m) {
+  return static_cast<int64_t>(G) * ((max_m + block_m - 1) / block_m) * block_m;
+}
+
+size_t w4a16_masked_workspace_size(int G, int max_m, int expected_m) {
+  if (G <= 0 || G > 1024 || max_m <= 0 || expected_m <= 0 ||
+      static_cast<int64_t>(G) * max_m >= (int64_t(1) << 31))
+    return 0;
+  const int bm = masked_block_m(expected_m);
+  return grouped_layout(masked_capacity(G, max_m, bm), bm).total;
+}
+
+w4a16_status_t w4a16_masked_gemm(const uint16_t* A, int64_t lda, int G, int max_m,
+                                 const int32_t* masked_m, int expected_m,
+                                 const w4a16_packed_weights_t* W, int epilogue, uint16_t* C,
+                                 int64_t ldc, void* workspace, size_t workspace_bytes,
+                                 int32_t* dev_err, w4a16_stream_t stream) {
+  w4a16_status_t st = check_packed(W);
+  if (st != W4A16_OK) return st;
+  if (G != W->E) return fail(W4A16_INVALID_ARG, "G (%d) must equal the weight's expert count (%d)", G, W->E);
+  if (G <= 0 || G > 1024 || max_m <= 0 || expected_m <= 0 ||
+      static_cast<int64_t>(G) * max_m >= (int64_t(1) << 31))
+    return fail(W4A16_INVALID_ARG, "need 1 <= G <= 1024, max_m > 0, expected_m > 0, G * max_m < 2^31");
+  if (!masked_m || !workspace || reinterpret_cast<uintptr_t>(workspace) % 256)
+    return fail(W4A16_INVALID_ARG, "masked_m and a 256-byte aligned workspace are required");
+  const int bm = masked_block_m(expected_m);
+  const int64_t cap = masked_capacity(G, max_m, bm);
+  const GroupedLayout L = grouped_layout(cap, bm);
+  if (workspace_bytes < L.total)
+    return fail(W4A16_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes", L.total);
+  DeviceFacts dev;
+  st = device_facts(&dev);
+  if (st != W4A16_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* sorted_ids = reinterpret_cast<int32_t*>(ws);
+  int32_t* expert_ids = reinterpret_cast<int32_t*>(ws + L.off_expert);
+  int32_t* ntp = reinterpret_cast<int32_t*>(ws + L.off_ntp);
+  cudaError_t err = launch_masked_layout(masked_m, G, max_m, bm, cap, sorted_ids, expert_ids, ntp,
+                                         dev_err, stream);
+  if (err != cudaSuccess) return cuda_fail(err, "masked layout launch");
+  const w4a16_routing_t R{sorted_ids, expert_ids, ntp, cap, bm, G * max_m};
+  const w4a16_schedule_t one_split{1, 0};
+  GemmCall c{A, lda, 1, W, &R, epilogue, 0u, C, ldc, nullptr, 0, expected_m, &one_split, dev_err, 0};
   return run_gemm(c, dev, stream);
 }
 
