@@ -62,6 +62,9 @@ def lib():
                                                 i32, i32, i32, vp, vp]),
                 "w4a16_oracle_contiguous_gemm": (i32, [vp, i64, i32, vp, vp, i32, i32, i32, vp, vp]),
                 "w4a16_oracle_masked_gemm": (i32, [vp, i32, i32, i32, vp, vp, i32, i32, vp, vp]),
+                "w4a16_oracle_nvfp4_dequant": (None, [vp, vp, i64, i32, vp]),
+                "w4a16_oracle_nvfp4_moe_gemm": (i32, [vp, i32, i32, vp, vp, i32, vp, vp, i32, i32,
+                                                      i32, i32, i32, vp, vp]),
                 "w4a16_oracle_silu_mul": (None, [vp, i64, i32, vp]),
                 "w4a16_oracle_topk_sum": (None, [vp, vp, vp, i32, i32, i32, vp]),
                 "w4a16_oracle_moe_layer": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
@@ -195,6 +198,48 @@ def moe_gemm(A, a_row_div: int, qweight, scales, sorted_ids, expert_ids, ntp: in
         bounds = [0, *[int(c) + 1 for c in cuts], E]
         bounds = sorted(set(min(max(b, 0), E) for b in bounds))
         with ThreadPoolExecutor(len(bounds) - 1) as ex:
+            list(ex.map(lambda lh: run(*lh), zip(bounds[:-1], bounds[1:])))
+    return torch.from_numpy(C) if out_f32 else _bf16_tensor(C)
+
+
+def nvfp4_dequant(codes, scales) -> torch.Tensor:
+    """NVFP4 codes uint8 [..., N, K/2] (element 2j in the low nibble), E4M3 scales uint8
+    [..., N, K/16] -> bf16 [..., N, K] (each weight the exact product)."""
+    c = _np(codes, np.uint8)
+    s = _np(scales, np.uint8)
+    K = c.shape[-1] * 2
+    rows = c.size // (K // 2)
+    out = np.empty(c.shape[:-1] + (K,), np.uint16)
+    lib().w4a16_oracle_nvfp4_dequant(_ptr(c), _ptr(s), rows, K, _ptr(out))
+    return _bf16_tensor(out)
+
+
+def nvfp4_moe_gemm(A, a_row_div: int, codes, scales, sorted_ids, expert_ids, ntp: int,
+                   block_m: int, total_slots: int, threads: int = 1,
+                   out_f32: bool = False) -> torch.Tensor:
+    """The indexed grouped GEMM with NVFP4 weights (codes [E, N, K/2], scales [E, N, K/16])."""
+    a = _np(A, np.uint16)
+    c = _np(codes, np.uint8)
+    s = _np(scales, np.uint8)
+    si = _np(sorted_ids, np.int32)
+    ei = _np(expert_ids, np.int32)
+    K = a.shape[-1]
+    E, N = c.shape[0], c.shape[1]
+    C = np.zeros((total_slots, N), np.float32 if out_f32 else np.uint16)
+    L = lib()
+
+    def run(lo, hi):
+        rc = L.w4a16_oracle_nvfp4_moe_gemm(_ptr(a), a_row_div, K, _ptr(c), _ptr(s), N, _ptr(si),
+                                           _ptr(ei), ntp, block_m, total_slots, lo, hi,
+                                           None if out_f32 else _ptr(C), _ptr(C) if out_f32 else None)
+        if rc:
+            raise ValueError(f"oracle nvfp4_moe_gemm failed with code {rc}")
+
+    if threads <= 1:
+        run(0, E)
+    else:
+        bounds = np.linspace(0, E, threads + 1).astype(int)
+        with ThreadPoolExecutor(threads) as ex:
             list(ex.map(lambda lh: run(*lh), zip(bounds[:-1], bounds[1:])))
     return torch.from_numpy(C) if out_f32 else _bf16_tensor(C)
 

@@ -127,6 +127,49 @@ void gemm_one_row(const uint16_t* a, int K, const int32_t* qweight, const uint16
   }
 }
 
+// ---- NVFP4 ("humans& Beats FlashInfer's Best MoE Kernel by 25% on Blackwell GPUs", "BF16
+// preserves each local product"): blocks of 16 E2M1 values along K share one E4M3 scale and a
+// weight is the product of the two, which BF16 represents exactly.
+
+// E2M1: sign bit 3, exponent bits 2..1 (bias 1), mantissa bit 0; exponent 0 is subnormal.
+double e2m1_value(unsigned code) {
+  const unsigned e = (code >> 1) & 3u, m = code & 1u;
+  const double mag = e == 0 ? 0.5 * m : std::ldexp(1.0 + 0.5 * m, static_cast<int>(e) - 1);
+  return (code & 8u) ? -mag : mag;
+}
+
+// E4M3 (the finite-only variant): sign bit 7, exponent bits 6..3 (bias 7), mantissa bits 2..0;
+// exponent 0 is subnormal, 0x7f / 0xff are NaN.
+double e4m3_value(unsigned byte) {
+  const unsigned e = (byte >> 3) & 15u, m = byte & 7u;
+  if (e == 15 && m == 7) return std::nan("");
+  const double mag = e == 0 ? std::ldexp(m / 8.0, -6) : std::ldexp(1.0 + m / 8.0, static_cast<int>(e) - 7);
+  return (byte & 0x80u) ? -mag : mag;
+}
+
+// Element k of one NVFP4 weight row (codes: two per byte, element 2j in the low nibble).
+float nvfp4_dequant_one(const uint8_t* crow, const uint8_t* srow, int k) {
+  const unsigned code = (crow[k / 2] >> (4 * (k % 2))) & 0xFu;
+  return bf16_to_float(double_to_bf16(e2m1_value(code) * e4m3_value(srow[k / 16])));
+}
+
+void gemm_one_row_nvfp4(const uint16_t* a, int K, const uint8_t* codes, const uint8_t* scales,
+                        int N, int e, uint16_t* out_row, float* out_f32) {
+  for (int n = 0; n < N; ++n) {
+    const uint8_t* crow = codes + (static_cast<int64_t>(e) * N + n) * (K / 2);
+    const uint8_t* srow = scales + (static_cast<int64_t>(e) * N + n) * (K / 16);
+    float acc = 0.0f;
+    for (int k = 0; k < K; ++k) {
+      const float p = bf16_to_float(a[k]) * nvfp4_dequant_one(crow, srow, k);
+      acc = acc + p;
+    }
+    if (out_f32)
+      out_f32[n] = acc;
+    else
+      out_row[n] = float_to_bf16(acc);
+  }
+}
+
 }  // namespace
 
 extern "C" {
@@ -257,6 +300,35 @@ void w4a16_oracle_topk_sum(const float* Y, const int32_t* topk_ids, const float*
       out[t * H + c] = double_to_bf16(acc);
     }
   }
+}
+
+// ---- NVFP4 weights ----------------------------------------------------------------
+
+// codes uint8 [rows, K/2], scales E4M3 [rows, K/16] -> BF16 [rows, K].
+void w4a16_oracle_nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, int64_t rows, int K,
+                                uint16_t* out) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int k = 0; k < K; ++k)
+      out[r * K + k] = float_to_bf16(nvfp4_dequant_one(codes + r * (K / 2), scales + r * (K / 16), k));
+}
+
+// The indexed grouped GEMM of w4a16_oracle_moe_gemm with NVFP4 weights.
+int w4a16_oracle_nvfp4_moe_gemm(const uint16_t* A, int a_row_div, int K, const uint8_t* codes,
+                                const uint8_t* scales, int N, const int32_t* sorted_ids,
+                                const int32_t* expert_ids, int num_tokens_padded, int block_m,
+                                int total_slots, int e_lo, int e_hi, uint16_t* C, float* C_f32) {
+  if (a_row_div <= 0 || K % 16 || block_m <= 0) return -3;
+  for (int64_t p = 0; p < num_tokens_padded; ++p) {
+    const int32_t i = sorted_ids[p];
+    if (i >= total_slots) continue;  // padding sentinel
+    const int32_t e = expert_ids[p / block_m];
+    if (e < e_lo || e >= e_hi) continue;
+    const uint16_t* a = A + static_cast<int64_t>(i / a_row_div) * K;
+    const int64_t row = static_cast<int64_t>(i) * N;
+    gemm_one_row_nvfp4(a, K, codes, scales, N, e, C_f32 ? nullptr : C + row,
+                       C_f32 ? C_f32 + row : nullptr);
+  }
+  return 0;
 }
 
 // ---- grouped contracts -------------------------------------------------------------

@@ -545,3 +545,85 @@ def test_masked_equals_contiguous_on_the_same_rows():
     Cc = oracle.contiguous_gemm(x, qw, sc, mi)
     valid = mi >= 0
     assert np.array_equal(bits(M[valid]), bits(Cc[valid]))
+
+
+# ---- NVFP4 weights ("humans& ...", "BF16 preserves each local product") ------------------
+
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]  # the E2M1 magnitudes of the OCP FP4 format
+
+
+def _nvfp4_all_pairs():
+    """One row per E4M3 scale byte: 16 codes x every scale, K = 16 per row."""
+    codes = np.zeros((256, 8), np.uint8)
+    for j in range(8):
+        codes[:, j] = (2 * j) | ((2 * j + 1) << 4)  # elements 0..15 = codes 0..15
+    scales = np.arange(256, dtype=np.uint8).reshape(256, 1)
+    return codes, scales
+
+
+def test_nvfp4_worked_product_from_the_pages():
+    # "the product 1.5 x 1.125 equals 1.6875; BF16 represents that value exactly"
+    with open(os.path.join(os.path.dirname(__file__), "golden", "bf16_exact_product.txt")) as f:
+        rows = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+    a, b, prod, bits_hex = rows[0][:4]
+    e2m1_code = E2M1_TABLE.index(float(a))           # 1.5 -> magnitude code 3
+    e4m3_byte = (7 << 3) | 1                          # 1.125 = 2^0 * (1 + 1/8)
+    assert float(b) == 1.125
+    codes = torch.tensor([[e2m1_code | (e2m1_code << 4)] * 8], dtype=torch.uint8)
+    scales = torch.tensor([[e4m3_byte]], dtype=torch.uint8)
+    wd = oracle.nvfp4_dequant(codes, scales)
+    assert float(wd[0, 0]) == float(prod)
+    assert int(wd.view(torch.int16)[0, 0]) & 0xFFFF == int(bits_hex, 16)
+
+
+def test_nvfp4_exhaustive_codes_times_every_e4m3_scale():
+    codes, scales = _nvfp4_all_pairs()
+    wd = oracle.nvfp4_dequant(torch.from_numpy(codes), torch.from_numpy(scales)).float().numpy()
+    s_lib = torch.from_numpy(scales.reshape(-1)).view(torch.float8_e4m3fn).float().numpy()  # library decode
+    for sb in range(256):
+        for c in range(16):
+            v = (-1.0 if c & 8 else 1.0) * E2M1_TABLE[c & 7]
+            exact = v * float(s_lib[sb])  # exact in float64
+            got = wd[sb, c]
+            if np.isnan(exact):
+                assert np.isnan(got)
+            else:
+                assert got == exact, (sb, c, got, exact)  # BF16 holds every product exactly
+
+
+def test_nvfp4_nibble_order_low_first_and_block_of_16():
+    codes = torch.zeros((1, 16), dtype=torch.uint8)
+    codes[0, 0] = 0x4 | (0x2 << 4)  # element 0 = 2.0, element 1 = 1.0
+    scales = torch.tensor([[7 << 3, 8 << 3]], dtype=torch.uint8)  # 1.0 for K 0..15, 2.0 for 16..31
+    codes[0, 8] = 0x2  # element 16 = 1.0 -> 2.0 after its block's scale
+    wd = oracle.nvfp4_dequant(codes, scales)[0].float()
+    assert wd[0] == 2.0 and wd[1] == 1.0 and wd[2] == 0.0 and wd[16] == 2.0 and wd[17] == 0.0
+
+
+def test_nvfp4_gemm_single_expert_equals_torch_matmul():
+    codes, scales = workloads.draw_nvfp4_weights(1, 64, 256, seed=41)
+    x = workloads.draw_activations(20, 256, seed=41)
+    ids = torch.zeros((20, 1), dtype=torch.int32)
+    s, e, ntp = oracle.moe_align(ids, 1, 16)
+    C = oracle.nvfp4_moe_gemm(x, 1, codes, scales, s, e, ntp, 16, 20).float()
+    ref = torch.matmul(x.float(), oracle.nvfp4_dequant(codes, scales)[0].float().T)
+    assert torch.all((C - ref).abs() <= torch.from_numpy(ulp_bf16(ref.numpy())).float() + 1e-6)
+
+
+def test_nvfp4_gemm_brute_force_per_token():
+    codes, scales = workloads.draw_nvfp4_weights(4, 48, 64, seed=42)
+    x = workloads.draw_activations(12, 64, seed=42)
+    ids, _ = workloads.draw_routing(12, 4, 2, seed=42)
+    s, e, ntp = oracle.moe_align(ids, 4, 4)
+    C = bf16_np(oracle.nvfp4_moe_gemm(x, 2, codes, scales, s, e, ntp, 4, 24))
+    # independent numpy decode of the codes and scales
+    c = codes.numpy()
+    nib = np.stack([c & 15, c >> 4], axis=-1).reshape(4, 48, 64)
+    mag = np.array(E2M1_TABLE)[nib & 7] * np.where(nib & 8, -1.0, 1.0)
+    sc = torch.from_numpy(scales.numpy().reshape(-1)).view(torch.float8_e4m3fn).double().numpy().reshape(4, 48, 4)
+    wd = mag * np.repeat(sc, 16, axis=-1)
+    xa = bf16_np(x)
+    for t in range(12):
+        for j in range(2):
+            ref = wd[int(ids[t, j])] @ xa[t]
+            assert np.all(np.abs(C[t * 2 + j] - ref) <= ulp_bf16(ref) + 1e-12)

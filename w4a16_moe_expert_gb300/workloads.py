@@ -109,6 +109,24 @@ def draw_weights(E: int, N: int, K: int, seed: int, group: int = GROUP):
     return qweight, scales
 
 
+def draw_nvfp4_weights(E: int, N: int, K: int, seed: int):
+    """NVFP4 weights: E2M1 codes two per byte along K (element 2j in the low nibble), uniform
+    over all 256 byte values, and one positive E4M3 scale byte per 16 K elements with an
+    exponent field of 1 or 2 and a uniform mantissa (scales in [2^-6, 2^-4 * 15/16]).
+
+    Returns ``(codes uint8 [E, N, K/2], scales uint8 [E, N, K/16])`` on the CPU.
+    """
+    if K % 16:
+        raise ValueError("K must be a multiple of 16")
+    rng = np.random.default_rng([seed, 3])
+    codes = rng.integers(0, 256, size=(E, N, K // 2), dtype=np.uint8)
+    rng_s = np.random.default_rng([seed, 4])
+    exp_field = rng_s.integers(1, 3, size=(E, N, K // 16), dtype=np.uint8)
+    mant = rng_s.integers(0, 8, size=(E, N, K // 16), dtype=np.uint8)
+    scales = (exp_field << 3) | mant
+    return torch.from_numpy(codes), torch.from_numpy(scales)
+
+
 def draw_activations(T: int, H: int, seed: int) -> torch.Tensor:
     """BF16 of N(0,1) draws, ``[T, H]`` on the CPU."""
     rng = np.random.default_rng([seed, 2])
