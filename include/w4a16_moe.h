@@ -102,6 +102,7 @@ w4a16_status_t w4a16_moe_align(const int32_t* topk_ids, int T, int top_k, int E,
  * 128 x 2 scales); chunks of one (e, j) are contiguous along K.
  * ---------------------------------------------------------------------------------------- */
 #define W4A16_PACK_GATE_UP_PAIRED 0x1u
+#define W4A16_PACK_NVFP4 0x2u /* set by w4a16_pack_weights_nvfp4: the blob holds NVFP4 weights */
 #define W4A16_PACK_MAGIC 0x3631413457454f4dull /* "MOEW4A16" in little-endian bytes */
 #define W4A16_PACK_VERSION 1u
 
@@ -119,6 +120,25 @@ w4a16_status_t w4a16_pack_weights(const int32_t* qweight, const uint16_t* scales
                                   int K, int group, uint32_t flags, void* packed,
                                   size_t packed_bytes, w4a16_packed_weights_t* desc,
                                   w4a16_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * NVFP4 weights ("humans& Beats FlashInfer's Best MoE Kernel by 25% on Blackwell GPUs", "BF16
+ * preserves each local product" and "Dedicated warps keep the pipeline busy"): blocks of 16
+ * E2M1 values along K share one E4M3 scale; the weight is their product, which BF16 holds
+ * exactly, so every GEMM and layer call runs unchanged on an NVFP4 blob (the descriptor's
+ * W4A16_PACK_NVFP4 flag selects the conversion; activations stay BF16).
+ *
+ * codes   device uint8 [E, N, K/2]: element k of a row in byte k/2, low nibble for even k;
+ *         E2M1 = sign bit 3, exponent bits 2..1 (bias 1), mantissa bit 0.
+ * scales  device uint8 [E, N, K/16]: E4M3 (finite variant, bias 7) of elements [16g, 16g+16).
+ * flags   0 or W4A16_PACK_GATE_UP_PAIRED (as above); the blob size is
+ *         w4a16_packed_bytes(E, N, K, 16, W4A16_PACK_NVFP4 | flags), the same as for INT4.
+ * A per-tensor FP32 second-level scale, where a checkpoint has one, is not part of this call
+ * (the pages do not use one): fold it into the activations or the consumer of the output.
+ * ---------------------------------------------------------------------------------------- */
+w4a16_status_t w4a16_pack_weights_nvfp4(const uint8_t* codes, const uint8_t* scales, int E, int N,
+                                        int K, uint32_t flags, void* packed, size_t packed_bytes,
+                                        w4a16_packed_weights_t* desc, w4a16_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
  * Indexed grouped GEMM ("Two kernel families"; "H200 and Blackwell indexed decode").

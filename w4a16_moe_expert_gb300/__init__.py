@@ -23,7 +23,7 @@ from . import build as _build
 
 __all__ = [
     "load", "library_path", "align_capacity", "moe_align", "PackedWeights", "pack_weights",
-    "Routing", "moe_gemm", "gather_rows", "contiguous_gemm", "masked_gemm", "topk_sum", "moe_layer", "layer_workspace_size", "plan_block_m",
+    "Routing", "pack_weights_nvfp4", "moe_gemm", "gather_rows", "contiguous_gemm", "masked_gemm", "topk_sum", "moe_layer", "layer_workspace_size", "plan_block_m",
     "plan_gemm", "debug_dequant", "gemm_workspace_size", "EPILOGUE_NONE", "EPILOGUE_SILU_MUL",
     "A_ROWS_SORTED", "C_ROWS_SORTED", "C_FP32", "PACK_GATE_UP_PAIRED", "LibraryError",
 ]
@@ -34,6 +34,7 @@ A_ROWS_SORTED = 0x1
 C_ROWS_SORTED = 0x2
 C_FP32 = 0x4
 PACK_GATE_UP_PAIRED = 0x1
+PACK_NVFP4 = 0x2
 PACK_MAGIC = 0x3631413457454F4D
 PACK_VERSION = 1
 
@@ -85,6 +86,7 @@ _SIGNATURES = {
     "w4a16_moe_align": (_I32, [_VP, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _I64, _I32, _VP, _VP]),
     "w4a16_packed_bytes": (_SZ, [_I32, _I32, _I32, _I32, _U32]),
     "w4a16_pack_weights": (_I32, [_VP, _VP, _I32, _I32, _I32, _I32, _U32, _VP, _SZ, _P(PackedDesc), _VP]),
+    "w4a16_pack_weights_nvfp4": (_I32, [_VP, _VP, _I32, _I32, _I32, _U32, _VP, _SZ, _P(PackedDesc), _VP]),
     "w4a16_gemm_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
     "w4a16_workspace_clear": (_I32, [_VP, _SZ, _VP]),
     "w4a16_moe_gemm": (_I32, [_VP, _I64, _I32, _P(PackedDesc), _P(RoutingDesc), _I32, _U32, _VP, _I64,
@@ -254,6 +256,26 @@ def pack_weights(qweight: torch.Tensor, scales: torch.Tensor, paired: bool = Fal
     _check("w4a16_pack_weights", load().w4a16_pack_weights(
         _ptr(qweight), _ptr(scales), E, N, K, 32, flags, _ptr(blob), nbytes, ctypes.byref(desc),
         _stream()))
+    return PackedWeights(blob, desc)
+
+
+def pack_weights_nvfp4(codes: torch.Tensor, scales: torch.Tensor, paired: bool = False) -> PackedWeights:
+    """Repack NVFP4 weights: uint8 [E, N, K/2] E2M1 codes (element 2j in the low nibble) and
+    uint8 [E, N, K/16] E4M3 scales, for the same GEMM and layer calls as INT4 weights."""
+    _cuda(codes, torch.uint8, "codes")
+    _cuda(scales, torch.uint8, "scales")
+    E, N, K2 = codes.shape
+    K = K2 * 2
+    if tuple(scales.shape) != (E, N, K // 16):
+        raise ValueError(f"scales must be [E, N, K/16] = {(E, N, K // 16)}, got {tuple(scales.shape)}")
+    flags = PACK_GATE_UP_PAIRED if paired else 0
+    nbytes = int(load().w4a16_packed_bytes(E, N, K, 16, flags | PACK_NVFP4))
+    if nbytes == 0:
+        raise LibraryError("w4a16_packed_bytes", 2, f"unsupported shape E={E} N={N} K={K}")
+    blob = torch.empty(nbytes, dtype=torch.uint8, device=codes.device)
+    desc = PackedDesc()
+    _check("w4a16_pack_weights_nvfp4", load().w4a16_pack_weights_nvfp4(
+        _ptr(codes), _ptr(scales), E, N, K, flags, _ptr(blob), nbytes, ctypes.byref(desc), _stream()))
     return PackedWeights(blob, desc)
 
 

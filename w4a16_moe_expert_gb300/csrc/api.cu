@@ -27,6 +27,8 @@ cudaError_t launch_contiguous_layout(const int32_t* m_indices, int m, int E, int
 cudaError_t launch_masked_layout(const int32_t* masked_m, int G, int max_m, int block_m,
                                  int64_t capacity, int32_t* sorted_ids, int32_t* expert_ids,
                                  int32_t* ntp, int32_t* dev_err, cudaStream_t stream);
+cudaError_t launch_pack_nvfp4(const uint8_t* codes, const uint8_t* scales, int E, int N, int K,
+                              uint32_t flags, void* packed, cudaStream_t stream);
 cudaError_t launch_pack(const int32_t* qweight, const uint16_t* scales, int E, int N, int K,
                         uint32_t flags, void* packed, cudaStream_t stream);
 cudaError_t launch_debug_dequant(const void* packed, int e, int N, int K, uint32_t flags,
@@ -95,8 +97,11 @@ static w4a16_status_t check_packed(const w4a16_packed_weights_t* W) {
   if (!W) return fail(W4A16_INVALID_ARG, "packed weight descriptor is NULL");
   if (W->magic != W4A16_PACK_MAGIC || W->version != W4A16_PACK_VERSION)
     return fail(W4A16_BAD_PACKED_WEIGHT, "packed weight descriptor has a bad magic or version");
-  if (W->group != 32 || W->K % kBlockK || W->N % kTileRows || W->E < 0 || !W->data)
+  const int group = (W->flags & W4A16_PACK_NVFP4) ? 16 : 32;
+  if (W->group != group || W->K % kBlockK || W->N % kTileRows || W->E < 0 || !W->data)
     return fail(W4A16_BAD_PACKED_WEIGHT, "packed weight descriptor has bad sizes");
+  if (W->flags & ~(W4A16_PACK_GATE_UP_PAIRED | W4A16_PACK_NVFP4))
+    return fail(W4A16_BAD_PACKED_WEIGHT, "packed weight descriptor has unknown flags");
   if (reinterpret_cast<uintptr_t>(W->data) % 256)
     return fail(W4A16_BAD_PACKED_WEIGHT, "packed weight blob must be 256-byte aligned");
   return W4A16_OK;
@@ -233,6 +238,7 @@ static w4a16_status_t run_gemm(const GemmCall& c, const DeviceFacts& dev, cudaSt
   a.n_tiles = c.W->N / kTileRows;
   a.n_kb = n_kb;
   a.paired = paired ? 1 : 0;
+  a.nvfp4 = (c.W->flags & W4A16_PACK_NVFP4) ? 1 : 0;
   a.sorted_ids = R->sorted_ids;
   a.expert_ids = R->expert_ids;
   a.ntp = R->num_tokens_padded;
@@ -308,8 +314,8 @@ w4a16_status_t w4a16_moe_align(const int32_t* topk_ids, int T, int top_k, int E,
 }
 
 size_t w4a16_packed_bytes(int E, int N, int K, int group, uint32_t flags) {
-  (void)flags;
-  if (E < 0 || N <= 0 || K <= 0 || group != 32 || K % kBlockK || N % kTileRows) return 0;
+  const int want = (flags & W4A16_PACK_NVFP4) ? 16 : 32;
+  if (E < 0 || N <= 0 || K <= 0 || group != want || K % kBlockK || N % kTileRows) return 0;
   return kHeaderBytes + static_cast<size_t>(E) * (N / kTileRows) * (K / kBlockK) * kChunkBytes;
 }
 
@@ -341,6 +347,39 @@ w4a16_status_t w4a16_pack_weights(const int32_t* qweight, const uint16_t* scales
   desc->N = N;
   desc->K = K;
   desc->group = group;
+  desc->bytes = need;
+  desc->data = packed;
+  return W4A16_OK;
+}
+
+w4a16_status_t w4a16_pack_weights_nvfp4(const uint8_t* codes, const uint8_t* scales, int E, int N,
+                                        int K, uint32_t flags, void* packed, size_t packed_bytes,
+                                        w4a16_packed_weights_t* desc, w4a16_stream_t stream) {
+  if (E < 0 || N <= 0 || K <= 0 || K % kBlockK || N % kTileRows)
+    return fail(W4A16_UNSUPPORTED, "need K %% 64 == 0 and N %% 128 == 0 (got N=%d K=%d)", N, K);
+  if (flags & ~W4A16_PACK_GATE_UP_PAIRED) return fail(W4A16_INVALID_ARG, "unknown pack flags");
+  if ((flags & W4A16_PACK_GATE_UP_PAIRED) && (N % 2 || (N / 2) % 64))
+    return fail(W4A16_UNSUPPORTED, "gate/up pairing needs I = N/2 to be a multiple of 64");
+  const uint32_t all = flags | W4A16_PACK_NVFP4;
+  const size_t need = w4a16_packed_bytes(E, N, K, 16, all);
+  if (!packed || !desc || (E > 0 && (!codes || !scales)))
+    return fail(W4A16_INVALID_ARG, "NULL pointer");
+  if (packed_bytes < need) return fail(W4A16_INVALID_ARG, "packed buffer needs %zu bytes", need);
+  if (reinterpret_cast<uintptr_t>(packed) % 256 || reinterpret_cast<uintptr_t>(codes) % 16 ||
+      reinterpret_cast<uintptr_t>(scales) % 4)
+    return fail(W4A16_INVALID_ARG, "packed must be 256-byte, codes 16-byte and scales 4-byte aligned");
+  DeviceFacts dev;
+  w4a16_status_t st = device_facts(&dev);
+  if (st != W4A16_OK) return st;
+  cudaError_t err = launch_pack_nvfp4(codes, scales, E, N, K, all, packed, stream);
+  if (err != cudaSuccess) return cuda_fail(err, "pack launch");
+  desc->magic = W4A16_PACK_MAGIC;
+  desc->version = W4A16_PACK_VERSION;
+  desc->flags = all;
+  desc->E = E;
+  desc->N = N;
+  desc->K = K;
+  desc->group = 16;
   desc->bytes = need;
   desc->data = packed;
   return W4A16_OK;

@@ -98,6 +98,64 @@ __device__ __forceinline__ void dequant_row64(uint4 lo, uint4 hi, uint32_t scale
   dequant_word(hi.w, s1, &r[28]);
 }
 
+// NVFP4 row of a 64-wide K block: 32 bytes of E2M1 pairs (element 2c in the low nibble of byte
+// c; bytes 0..15 in lo, 16..31 in hi) and four E4M3 scales (one per 16 elements, byte i of
+// scales4) -> 32 BF16x2 registers in K order.  Every product of an E2M1 value and an E4M3 scale
+// is exact in BF16, and so is each step: the E2M1 pair converts to FP16 exactly (the
+// e2m1x2 -> f16x2 conversion), the FP16 bits shifted right by 3 (sign kept) are the BF16 bits
+// of the same value times 2^-112, and the scale is taken as BF16 times 2^112, so the one
+// BF16 multiply yields the exact product.
+__device__ __forceinline__ void nvfp4_scales(uint32_t scales4, uint32_t (&sb)[4]) {
+  uint32_t f01, f23;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f01) : "h"(static_cast<uint16_t>(scales4 & 0xFFFFu)));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f23) : "h"(static_cast<uint16_t>(scales4 >> 16)));
+  const uint32_t f[2] = {f01, f23};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint16_t b;
+    asm("cvt.rn.bf16.f16 %0, %1;" : "=h"(b) : "h"(static_cast<uint16_t>(f[i >> 1] >> (16 * (i & 1)))));
+    const uint32_t pair = static_cast<uint32_t>(b) * 0x00010001u;  // the scale in both halves
+    uint32_t scaled;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(scaled) : "r"(pair), "r"(0x77807780u));  // x 2^112
+    sb[i] = scaled;
+  }
+}
+
+// Four E2M1 pairs of one word -> four BF16x2 products with the (2^112-scaled) scale pair sb.
+__device__ __forceinline__ void nvfp4_word(uint32_t word, uint32_t sb, uint32_t* out) {
+  uint32_t h0, h1, h2, h3;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+      : "r"(word));
+  const uint32_t h[4] = {h0, h1, h2, h3};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t v = ((h[i] & 0x7FFF7FFFu) >> 3) | (h[i] & 0x80008000u);  // BF16 of value * 2^-112
+    uint32_t w;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(w) : "r"(v), "r"(sb));
+    out[i] = w;
+  }
+}
+
+__device__ __forceinline__ void dequant_row64_nvfp4(uint4 lo, uint4 hi, uint32_t scales4,
+                                                    uint32_t (&r)[32]) {
+  uint32_t sb[4];
+  nvfp4_scales(scales4, sb);
+  nvfp4_word(lo.x, sb[0], &r[0]);  // elements 0..7
+  nvfp4_word(lo.y, sb[0], &r[4]);  // 8..15
+  nvfp4_word(lo.z, sb[1], &r[8]);  // 16..23
+  nvfp4_word(lo.w, sb[1], &r[12]);
+  nvfp4_word(hi.x, sb[2], &r[16]);  // 32..39
+  nvfp4_word(hi.y, sb[2], &r[20]);
+  nvfp4_word(hi.z, sb[3], &r[24]);
+  nvfp4_word(hi.w, sb[3], &r[28]);
+}
+
 // ---- mbarrier ------------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -538,12 +538,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&aempty[sa]), pa ^ 1, abort_flag, a.dev_err)))
           goto dq_done;
         tc_fence_after();
+        if (a.nvfp4) {
 #pragma unroll
-        for (int sb = 0; sb < KS; ++sb) {
-          if (sb < nsub) {
-            uint32_t v[32];
-            dequant_row64(lo[sb], hi[sb], s2[sb], v);
-            tmem_st32(lane_base + sa * (KS * 32) + sb * 32, v);
+          for (int sb = 0; sb < KS; ++sb) {
+            if (sb < nsub) {
+              uint32_t v[32];
+              dequant_row64_nvfp4(lo[sb], hi[sb], s2[sb], v);
+              tmem_st32(lane_base + sa * (KS * 32) + sb * 32, v);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int sb = 0; sb < KS; ++sb) {
+            if (sb < nsub) {
+              uint32_t v[32];
+              dequant_row64(lo[sb], hi[sb], s2[sb], v);
+              tmem_st32(lane_base + sa * (KS * 32) + sb * 32, v);
+            }
           }
         }
         tmem_wait_st();

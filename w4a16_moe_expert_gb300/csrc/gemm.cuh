@@ -16,6 +16,7 @@ struct GemmArgs {
   const uint8_t* wblob;
   int E, N, K, n_tiles, n_kb;
   int paired;
+  int nvfp4;  // the blob holds NVFP4 (E2M1 + E4M3 per 16) weights instead of INT4
   const int32_t* sorted_ids;
   const int32_t* expert_ids;
   const int32_t* ntp;

@@ -9,6 +9,8 @@
 //   bytes [4096, 4608)  row r at 4096 + 4*r: the two BF16 scales of the block
 // Words are nibble-interleaved (positions 0..3 hold elements 0,2,4,6 and 4..7 hold 1,3,5,7)
 // so that one mask yields two neighbouring elements in the two halves of a register.
+// NVFP4 blobs use the same chunk geometry with the codes in their natural byte order (one
+// byte = one E2M1 pair, which the hardware converts as a pair) and four E4M3 scales per row.
 #include "common.cuh"
 
 namespace w4a16 {
@@ -33,6 +35,23 @@ __global__ void __launch_bounds__(kTileRows)
   reinterpret_cast<uint32_t*>(chunk + kScaleOffset)[r] = s2;
 }
 
+// NVFP4 (one thread per tile row): the row's 32 code bytes of the K block in order (bytes
+// 0..15 at 16*r, 16..31 at 2048 + 16*r) and its four E4M3 scale bytes at 4096 + 4*r.
+__global__ void __launch_bounds__(kTileRows)
+    pack_nvfp4_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales, int N,
+                      int K, int n_tiles, int n_kb, int paired, uint8_t* __restrict__ out) {
+  const int kb = blockIdx.x, j = blockIdx.y, e = blockIdx.z, r = threadIdx.x;
+  const int n = tile_row_to_canonical(j, r, N, paired != 0);
+  const int64_t row = static_cast<int64_t>(e) * N + n;
+  const uint4* src = reinterpret_cast<const uint4*>(codes + row * (K / 2) + kb * 32);
+  const uint32_t s4 = __ldg(reinterpret_cast<const uint32_t*>(scales + row * (K / 16) + kb * 4));
+  uint8_t* chunk =
+      out + kHeaderBytes + ((static_cast<int64_t>(e) * n_tiles + j) * n_kb + kb) * kChunkBytes;
+  reinterpret_cast<uint4*>(chunk)[r] = __ldg(src);
+  reinterpret_cast<uint4*>(chunk + kCodeHalfBytes)[r] = __ldg(src + 1);
+  reinterpret_cast<uint32_t*>(chunk + kScaleOffset)[r] = s4;
+}
+
 __global__ void write_header_kernel(PackedHeader h, uint8_t* out) {
   *reinterpret_cast<PackedHeader*>(out) = h;
 }
@@ -40,7 +59,7 @@ __global__ void write_header_kernel(PackedHeader h, uint8_t* out) {
 // Debug: dequantise expert e back to canonical [N, K] with the GEMM's conversion routine.
 __global__ void __launch_bounds__(kTileRows)
     debug_dequant_kernel(const uint8_t* __restrict__ packed, int e, int N, int K, int n_tiles,
-                         int n_kb, int paired, uint16_t* __restrict__ out) {
+                         int n_kb, int paired, int nvfp4, uint16_t* __restrict__ out) {
   const int kb = blockIdx.x, j = blockIdx.y, r = threadIdx.x;
   const uint8_t* chunk =
       packed + kHeaderBytes + ((static_cast<int64_t>(e) * n_tiles + j) * n_kb + kb) * kChunkBytes;
@@ -48,7 +67,10 @@ __global__ void __launch_bounds__(kTileRows)
   const uint4 hi = reinterpret_cast<const uint4*>(chunk + kCodeHalfBytes)[r];
   const uint32_t s2 = reinterpret_cast<const uint32_t*>(chunk + kScaleOffset)[r];
   uint32_t v[32];
-  dequant_row64(lo, hi, s2, v);
+  if (nvfp4)
+    dequant_row64_nvfp4(lo, hi, s2, v);
+  else
+    dequant_row64(lo, hi, s2, v);
   const int n = tile_row_to_canonical(j, r, N, paired != 0);
   uint4* dst = reinterpret_cast<uint4*>(out + static_cast<int64_t>(n) * K + kb * kBlockK);
 #pragma unroll
@@ -78,12 +100,35 @@ cudaError_t launch_pack(const int32_t* qweight, const uint16_t* scales, int E, i
   return cudaGetLastError();
 }
 
+cudaError_t launch_pack_nvfp4(const uint8_t* codes, const uint8_t* scales, int E, int N, int K,
+                              uint32_t flags, void* packed, cudaStream_t stream) {
+  const int n_tiles = N / kTileRows, n_kb = K / kBlockK;
+  PackedHeader h{};
+  h.magic = W4A16_PACK_MAGIC;
+  h.version = W4A16_PACK_VERSION;
+  h.flags = flags;
+  h.E = E;
+  h.N = N;
+  h.K = K;
+  h.group = 16;
+  h.n_tiles = n_tiles;
+  h.n_kb = n_kb;
+  uint8_t* out = static_cast<uint8_t*>(packed);
+  write_header_kernel<<<1, 1, 0, stream>>>(h, out);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  if (E == 0) return cudaSuccess;
+  pack_nvfp4_kernel<<<dim3(n_kb, n_tiles, E), kTileRows, 0, stream>>>(
+      codes, scales, N, K, n_tiles, n_kb, (flags & W4A16_PACK_GATE_UP_PAIRED) ? 1 : 0, out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_debug_dequant(const void* packed, int e, int N, int K, uint32_t flags,
                                  uint16_t* out, cudaStream_t stream) {
   const int n_tiles = N / kTileRows, n_kb = K / kBlockK;
   debug_dequant_kernel<<<dim3(n_kb, n_tiles), kTileRows, 0, stream>>>(
       static_cast<const uint8_t*>(packed), e, N, K, n_tiles, n_kb,
-      (flags & W4A16_PACK_GATE_UP_PAIRED) ? 1 : 0, out);
+      (flags & W4A16_PACK_GATE_UP_PAIRED) ? 1 : 0, (flags & W4A16_PACK_NVFP4) ? 1 : 0, out);
   return cudaGetLastError();
 }
 
