@@ -341,6 +341,105 @@ def run_ours(args, rank, world, local_rank):
     call_us = [(statistics.median(g), statistics.median(d)) for g, d in bb_samples]
     step_ms = wall / args.steps * 1e3
 
+    # ---- the other weight format and the grouped contracts (per-call, same method) ----
+    def per_call_us(fn, n):
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize()
+        if use_graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(n):
+                    fn(i)
+            run = g.replay
+        else:
+            def run():
+                for i in range(n):
+                    fn(i)
+        run()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(max(5, min(args.steps, 20))):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            run()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3 / n)
+        return statistics.median(ts)
+
+    extras = {}
+    if not args.no_extras:
+        from w4a16_moe_expert_gb300.workloads import draw_nvfp4_weights
+        c13, s13 = draw_nvfp4_weights(wl.E, 2 * wl.I, wl.H, seed=100 * 2 + 7)
+        c2, s2 = draw_nvfp4_weights(wl.E, wl.H, wl.I, seed=100 * 2 + 8)
+        f13 = [lib.pack_weights_nvfp4(c13.to(dev), s13.to(dev), paired=True)]
+        f2 = [lib.pack_weights_nvfp4(c2.to(dev), s2.to(dev))]
+        del c13, s13, c2, s2
+        f13 += [f13[0].clone() for _ in range(len(w13s) - 1)]
+        f2 += [f2[0].clone() for _ in range(len(w2s) - 1)]
+        rows = []
+        for c in cases:
+            a = c["acct"]
+            gu = per_call_us(lambda i: gate_up_call(c, f13[i % c["n_gu"]]), c["R_gu"])
+            dn = per_call_us(lambda i: down_call(c, f2[i % c["n_dn"]]), c["R_dn"])
+            rows.append({"T": c["T"], "gate_up_us": round(gu, 2), "down_us": round(dn, 2),
+                         "gate_up_weight_GBps": round(a["gate_up"]["weight_bytes"] / gu / 1e3, 1),
+                         "down_weight_GBps": round(a["down"]["weight_bytes"] / dn / 1e3, 1)})
+        extras["nvfp4_weights"] = {
+            "what": "the same sweep with NVFP4 weights (E2M1, E4M3 scale per 16 K; BF16 activations)",
+            "sweep": rows}
+        del f13, f2
+
+        # grouped contracts on the routings of the largest and of a decode-sized T
+        big = max(cases, key=lambda c: c["T"])
+        small = min((c for c in cases if c["T"] >= 8), key=lambda c: abs(c["T"] - 64), default=None)
+        ids_b = big["ids"].reshape(-1).cpu()
+        counts = torch.bincount(ids_b[ids_b >= 0], minlength=wl.E)
+        order = torch.argsort(ids_b, stable=True)
+        rows_idx, mi = [], []
+        pos = 0
+        for e_, cnt in enumerate(counts.tolist()):
+            sel = order[pos:pos + cnt]
+            pos += cnt
+            rows_idx += (sel // wl.top_k).tolist() + [0] * ((-cnt) % 128)
+            mi += [e_] * cnt + [-1] * ((-cnt) % 128)
+        A_c = big["x"][torch.tensor(rows_idx, device=dev)].contiguous()
+        mi_d = torch.tensor(mi, dtype=torch.int32, device=dev)
+        out_c = torch.empty((A_c.shape[0], wl.I), dtype=torch.bfloat16, device=dev)
+        ws_c = torch.empty(int(lib.load().w4a16_contiguous_workspace_size(A_c.shape[0])),
+                           dtype=torch.uint8, device=dev)
+        t_c = per_call_us(lambda i: lib.contiguous_gemm(A_c, w13s[i % big["n_gu"]], mi_d, epilogue=1,
+                                                        out=out_c, workspace=ws_c), big["R_gu"])
+        grouped = {"contiguous_gate_up": {
+            "T": big["T"], "m": int(A_c.shape[0]), "us": round(t_c, 2),
+            "weight_GBps": round(big["acct"]["gate_up"]["weight_bytes"] / t_c / 1e3, 1),
+            "TFLOPs": round(big["acct"]["gate_up"]["flops"] / t_c / 1e6, 1)}}
+        if small is not None:
+            ids_s = small["ids"].cpu()
+            cnt_s = torch.bincount(ids_s.reshape(-1)[ids_s.reshape(-1) >= 0], minlength=wl.E)
+            max_m = int(max(16, (int(cnt_s.max()) + 15) // 16 * 16))
+            fill = [0] * wl.E
+            tok = torch.zeros((wl.E, max_m), dtype=torch.long)  # token of (expert, row)
+            for t_, row in enumerate(ids_s.tolist()):
+                for e_ in row:
+                    if e_ >= 0:
+                        tok[e_, fill[e_]] = t_
+                        fill[e_] += 1
+            A_m = small["x"][tok.reshape(-1).to(dev)].reshape(wl.E, max_m, wl.H).contiguous()
+            mm = cnt_s.to(torch.int32).to(dev)
+            exp_m = max(1, round(small["T"] * wl.top_k / wl.E))
+            out_m = torch.empty((wl.E * max_m, wl.I), dtype=torch.bfloat16, device=dev)
+            ws_m = torch.empty(int(lib.load().w4a16_masked_workspace_size(wl.E, max_m, exp_m)),
+                               dtype=torch.uint8, device=dev)
+            t_m = per_call_us(lambda i: lib.masked_gemm(A_m, w13s[i % small["n_gu"]], mm, exp_m,
+                                                        epilogue=1, out=out_m, workspace=ws_m),
+                              small["R_gu"])
+            grouped["masked_gate_up"] = {
+                "T": small["T"], "G": wl.E, "max_m": max_m, "expected_m": exp_m, "us": round(t_m, 2),
+                "weight_GBps": round(small["acct"]["gate_up"]["weight_bytes"] / t_m / 1e3, 1)}
+        extras["grouped_contracts"] = grouped
+
     # e2e through the public layer call, host buffers, copies inside the timed region
     e2e_events = []
     h2d = sum(c["x_h"].numel() * 2 + c["ids_h"].numel() * 4 + c["w_h"].numel() * 4 for c in cases)
@@ -428,6 +527,7 @@ def run_ours(args, rank, world, local_rank):
                        "every layer stage"),
             "parallelism": "replicas" if world > 1 else "single GPU",
             "sweep": sweep,
+            **extras,
         },
         "roofline": {
             "bound": "hbm",
@@ -531,6 +631,8 @@ def main():
     ap.add_argument("--ref-step-budget", type=float, default=4.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of a graph")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the NVFP4 and grouped-contract measurements")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps are required")
