@@ -291,6 +291,15 @@ w4a16_status_t w4a16_topk_sum(const float* Y, const int32_t* topk_ids,
  * used only for the schedule.  block_m: 0 = planner.  workspace of
  * w4a16_layer_workspace_size(..) bytes with the same block_m argument; no zeroing needed.
  * ---------------------------------------------------------------------------------------- */
+/* Layer options.  W4A16_LAYER_FUSED_TOPK: the down GEMM's epilogue multiplies each slot's row
+ * by its top-k weight and adds it into an FP32 [T, H] token sum with atomic vector reductions
+ * (the per-slot [T*top_k, H] rows are never written), and a last kernel rounds the sums to BF16
+ * ("humans& ...", "Dedicated warps keep the pipeline busy": the top-K expert output merge in the
+ * MoE kernel).  Six kernels instead of five: a zeroing kernel precedes the GEMMs.  The order in
+ * which the slots' terms are added then varies from run to run, so results are within the
+ * tolerance but not bitwise reproducible; without the flag the sum runs over slots in order
+ * and is reproducible. */
+#define W4A16_LAYER_FUSED_TOPK 0x1u
 int w4a16_plan_block_m(int T, int top_k, int E, int E_global);
 size_t w4a16_layer_workspace_size(int T, int top_k, int E, int E_global, int H, int I,
                                   int block_m);
@@ -299,6 +308,12 @@ w4a16_status_t w4a16_moe_layer(const uint16_t* x, const w4a16_packed_weights_t* 
                                const float* topk_weights, int T, int top_k, int E_global,
                                int block_m, uint16_t* out, void* workspace,
                                size_t workspace_bytes, int32_t* dev_err, w4a16_stream_t stream);
+w4a16_status_t w4a16_moe_layer_ex(const uint16_t* x, const w4a16_packed_weights_t* w13,
+                                  const w4a16_packed_weights_t* w2, const int32_t* topk_ids,
+                                  const float* topk_weights, int T, int top_k, int E_global,
+                                  int block_m, uint32_t layer_flags, uint16_t* out,
+                                  void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                                  w4a16_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
  * Host planner (no device work; usable without a GPU): the schedule w4a16_moe_gemm would

@@ -35,6 +35,7 @@ C_ROWS_SORTED = 0x2
 C_FP32 = 0x4
 PACK_GATE_UP_PAIRED = 0x1
 PACK_NVFP4 = 0x2
+LAYER_FUSED_TOPK = 0x1
 PACK_MAGIC = 0x3631413457454F4D
 PACK_VERSION = 1
 
@@ -105,6 +106,8 @@ _SIGNATURES = {
     "w4a16_layer_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32, _I32]),
     "w4a16_moe_layer": (_I32, [_VP, _P(PackedDesc), _P(PackedDesc), _VP, _VP, _I32, _I32, _I32, _I32,
                                _VP, _VP, _SZ, _VP, _VP]),
+    "w4a16_moe_layer_ex": (_I32, [_VP, _P(PackedDesc), _P(PackedDesc), _VP, _VP, _I32, _I32, _I32, _I32,
+                                  _U32, _VP, _VP, _SZ, _VP, _VP]),
     "w4a16_plan_gemm": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _P(PlanDesc)]),
     "w4a16_debug_dequant": (_I32, [_P(PackedDesc), _I32, _VP, _VP]),
 }
@@ -435,7 +438,9 @@ def layer_workspace_size(T: int, top_k: int, E: int, H: int, I: int, E_global: i
 def moe_layer(x: torch.Tensor, w13: PackedWeights, w2: PackedWeights, topk_ids: torch.Tensor,
               topk_weights: torch.Tensor, E_global: int = 0, block_m: int = 0,
               out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-              dev_err: Optional[torch.Tensor] = None) -> torch.Tensor:
+              dev_err: Optional[torch.Tensor] = None, fused_topk: bool = False) -> torch.Tensor:
+    """The whole layer; ``fused_topk`` merges the top-k outputs inside the down GEMM
+    (atomic FP32 sums: within the tolerance, not bitwise reproducible)."""
     _cuda(x, torch.bfloat16, "x")
     _cuda(topk_ids, torch.int32, "topk_ids")
     _cuda(topk_weights, torch.float32, "topk_weights")
@@ -446,10 +451,10 @@ def moe_layer(x: torch.Tensor, w13: PackedWeights, w2: PackedWeights, topk_ids: 
     need = layer_workspace_size(T, k, w13.E, H, w13.N // 2, E_global, block_m)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
-    _check("w4a16_moe_layer", load().w4a16_moe_layer(
+    _check("w4a16_moe_layer_ex", load().w4a16_moe_layer_ex(
         _ptr(x), ctypes.byref(w13.desc), ctypes.byref(w2.desc), _ptr(topk_ids), _ptr(topk_weights),
-        T, k, E_global, block_m, _ptr(out), _ptr(workspace), workspace.numel(), _ptr(dev_err),
-        _stream()))
+        T, k, E_global, block_m, LAYER_FUSED_TOPK if fused_topk else 0, _ptr(out), _ptr(workspace),
+        workspace.numel(), _ptr(dev_err), _stream()))
     return out
 
 

@@ -161,6 +161,60 @@ static cudaError_t launch_topk_sum(const float* Y, const int32_t* ids, const flo
   return cudaLaunchKernelEx(&cfg, topk_sum_kernel, Y, ids, w, T, top_k, H, out);
 }
 
+// ---- fused top-k merge helpers: zero the FP32 token sums, then round them to BF16 ------------
+__global__ void __launch_bounds__(256) zero_f32_kernel(float* __restrict__ p, int64_t n4) {
+  pdl_wait();  // the previous call's last kernel may still read this buffer
+  pdl_launch_dependents();
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    reinterpret_cast<float4*>(p)[i] = z;
+}
+
+__global__ void __launch_bounds__(256)
+    round_bf16_kernel(const float* __restrict__ acc, int64_t n8, uint16_t* __restrict__ out) {
+  pdl_wait();  // the sums come from the down GEMM
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+    auto pk = [](float lo, float hi) {
+      return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+             (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+    };
+    reinterpret_cast<uint4*>(out)[i] = make_uint4(pk(a.x, a.y), pk(a.z, a.w), pk(b.x, b.y), pk(b.z, b.w));
+  }
+}
+
+// A grid-stride launch of 256-thread blocks with programmatic dependent launch.
+static void pdl_config(int64_t work_items, int num_sms, cudaStream_t stream, cudaLaunchConfig_t* cfg,
+                       cudaLaunchAttribute* attr) {
+  *cfg = {};
+  const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((work_items + 255) / 256, num_sms * 8));
+  cfg->gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg->blockDim = dim3(256);
+  cfg->stream = stream;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg->attrs = attr;
+  cfg->numAttrs = 1;
+}
+
+static cudaError_t launch_zero_f32(float* p, int64_t n, int num_sms, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  pdl_config(n / 4, num_sms, stream, &cfg, attr);
+  return cudaLaunchKernelEx(&cfg, zero_f32_kernel, p, n / 4);
+}
+
+static cudaError_t launch_round_bf16(const float* acc, int64_t n, uint16_t* out, int num_sms,
+                                     cudaStream_t stream) {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  pdl_config(n / 8, num_sms, stream, &cfg, attr);
+  return cudaLaunchKernelEx(&cfg, round_bf16_kernel, acc, n / 8, out);
+}
+
 // ---- GEMM call shared by the ABI entry and the layer ----------------------------------------------
 struct GemmCall {
   const uint16_t* A;
@@ -178,6 +232,8 @@ struct GemmCall {
   const w4a16_schedule_t* sched;
   int32_t* dev_err;
   int routing_ready;
+  const float* merge_w = nullptr;  // fused top-k merge (C = FP32 token sums)
+  int merge_k = 0;
 };
 
 static w4a16_status_t run_gemm(const GemmCall& c, const DeviceFacts& dev, cudaStream_t stream) {
@@ -258,6 +314,8 @@ static w4a16_status_t run_gemm(const GemmCall& c, const DeviceFacts& dev, cudaSt
   // weights streamed once per call (few rows per expert) are marked evict-first in L2
   a.evict_first = (c.rows_hint > 0 ? c.rows_hint : R->total_slots / std::max(1, c.W->E)) <= R->block_m;
   a.routing_ready = c.routing_ready;
+  a.merge_w = c.merge_w;
+  a.merge_k = c.merge_k;
   cudaError_t err = launch_gemm(a, grid, true, stream);
   if (err != cudaSuccess) return cuda_fail(err, "moe_gemm launch");
   return W4A16_OK;
@@ -629,6 +687,18 @@ w4a16_status_t w4a16_moe_layer(const uint16_t* x, const w4a16_packed_weights_t* 
                                const float* topk_weights, int T, int top_k, int E_global,
                                int block_m, uint16_t* out, void* workspace,
                                size_t workspace_bytes, int32_t* dev_err, w4a16_stream_t stream) {
+  return w4a16_moe_layer_ex(x, w13, w2, topk_ids, topk_weights, T, top_k, E_global, block_m, 0u,
+                            out, workspace, workspace_bytes, dev_err, stream);
+}
+
+w4a16_status_t w4a16_moe_layer_ex(const uint16_t* x, const w4a16_packed_weights_t* w13,
+                                  const w4a16_packed_weights_t* w2, const int32_t* topk_ids,
+                                  const float* topk_weights, int T, int top_k, int E_global,
+                                  int block_m, uint32_t layer_flags, uint16_t* out,
+                                  void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                                  w4a16_stream_t stream) {
+  if (layer_flags & ~W4A16_LAYER_FUSED_TOPK) return fail(W4A16_INVALID_ARG, "unknown layer flags");
+  const bool fused = (layer_flags & W4A16_LAYER_FUSED_TOPK) != 0;
   w4a16_status_t st = check_packed(w13);
   if (st != W4A16_OK) return st;
   if ((st = check_packed(w2)) != W4A16_OK) return st;
@@ -666,6 +736,10 @@ w4a16_status_t w4a16_moe_layer(const uint16_t* x, const w4a16_packed_weights_t* 
                                      reinterpret_cast<int32_t*>(ws + L.off_cnt),
                                      static_cast<int>(split_unit_budget(L.block_m)), stream);
   if (err != cudaSuccess) return cuda_fail(err, "moe_align launch");
+  if (fused) {  // the down GEMM adds into FP32 token sums held where the per-slot rows would be
+    err = launch_zero_f32(y, static_cast<int64_t>(T) * H, dev.num_sms, stream);
+    if (err != cudaSuccess) return cuda_fail(err, "zero launch");
+  }
 
   w4a16_routing_t R{sorted_ids, expert_ids, ntp, L.cap, L.block_m, n_slots};
   const int eg = E_global > 0 ? E_global : E;
@@ -687,6 +761,16 @@ w4a16_status_t w4a16_moe_layer(const uint16_t* x, const w4a16_packed_weights_t* 
   GemmCall g2{h, I, 1, w2, &R, W4A16_EPILOGUE_NONE, W4A16_A_ROWS_SORTED | W4A16_C_FP32,
               reinterpret_cast<uint16_t*>(y), H,
               ws + L.off_cnt, (L.off_xs - L.off_cnt), rows_hint, nullptr, dev_err, 1};
+  if (fused) {
+    const w4a16_schedule_t one_split{1, 0};  // the merge is the reduction: no K splits
+    g2.sched = &one_split;
+    g2.merge_w = topk_weights;
+    g2.merge_k = top_k;
+    if ((st = run_gemm(g2, dev, stream)) != W4A16_OK) return st;
+    err = launch_round_bf16(y, static_cast<int64_t>(T) * H, out, dev.num_sms, stream);
+    if (err != cudaSuccess) return cuda_fail(err, "round launch");
+    return W4A16_OK;
+  }
   if ((st = run_gemm(g2, dev, stream)) != W4A16_OK) return st;
   err = launch_topk_sum(y, topk_ids, topk_weights, T, top_k, H, out, stream);
   if (err != cudaSuccess) return cuda_fail(err, "topk_sum launch");

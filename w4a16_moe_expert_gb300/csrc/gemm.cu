@@ -162,7 +162,20 @@ __device__ __forceinline__ void store_chunk16(const GemmArgs& a, const Unit& un,
     if (row >= 0) {
       const int col = tile_row_to_canonical(un.jt, 32 * q + 16 * half, a.N, a.paired != 0);
       const float4* src = reinterpret_cast<const float4*>(st + tok * 32 + 16 * half);
-      if (a.c_f32) {
+      if (a.merge_w) {
+        // top-k merge: this slot's weighted row is added into its token's FP32 row
+        if (routed) {
+          const float w = __ldg(a.merge_w + slot);
+          float* dst = reinterpret_cast<float*>(a.C) + static_cast<int64_t>(slot / a.merge_k) * a.ldc + col;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float4 v = src[k];
+            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4 * k),
+                         "f"(w * v.x), "f"(w * v.y), "f"(w * v.z), "f"(w * v.w)
+                         : "memory");
+          }
+        }
+      } else if (a.c_f32) {
         float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.C) + row * a.ldc + col);
 #pragma unroll
         for (int k = 0; k < 4; ++k) dst[k] = routed ? src[k] : make_float4(0.f, 0.f, 0.f, 0.f);

@@ -26,6 +26,8 @@ struct GemmArgs {
   int epilogue;
   int c_sorted;
   int c_f32;  // C is float (unrounded sums)
+  const float* merge_w;  // non-null: add merge_w[slot] * value into C row slot / merge_k (FP32)
+  int merge_k;
   uint16_t* C;
   int64_t ldc;
   float* part;
