@@ -500,14 +500,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const float* tile_parts = a.part + un.tile * split_k * (128 * NT);
 #pragma unroll 1
           for (int c0 = 0; c0 < NT; c0 += 16) {
+            // splits summed in order; the 16 columns of one split load together
+            float v[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) v[jj] = __ldcg(tile_parts + (c0 + jj) * 128 + t);
+            for (int s = 1; s < split_k; ++s) {
+              float w[16];
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj)
+                w[jj] = __ldcg(tile_parts + s * (128 * NT) + (c0 + jj) * 128 + t);
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj) v[jj] += w[jj];
+            }
             uint32_t r[16];
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-              float v = 0.0f;
-              for (int s = 0; s < split_k; ++s)
-                v += __ldcg(tile_parts + s * (128 * NT) + (c0 + jj) * 128 + t);
-              r[jj] = __float_as_uint(v);
-            }
+            for (int jj = 0; jj < 16; ++jj) r[jj] = __float_as_uint(v[jj]);
             store_chunk16(a, un, q, lane, c0, epi_rows, r, epi_stage);
           }
           if (t == 0) a.cnt[un.tile] = 0;  // ready for the next call
