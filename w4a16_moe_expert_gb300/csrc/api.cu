@@ -267,6 +267,8 @@ static w4a16_status_t run_gemm(const GemmCall& c, const DeviceFacts& dev, cudaSt
     return fail(W4A16_INVALID_ARG, "FP32 output is available with epilogue NONE only");
   if (R->capacity == 0 || c.W->E == 0) return W4A16_OK;
 
+  if ((R->capacity / R->block_m) * static_cast<int64_t>(c.W->N / kTileRows) * 16 >= (int64_t(1) << 31))
+    return fail(W4A16_UNSUPPORTED, "routing capacity too large for one call (units must stay below 2^31)");
   w4a16_plan_t plan;
   plan_gemm(R->total_slots, c.W->E, c.W->N, c.W->K, R->block_m, c.rows_hint, dev.num_sms, &plan);
   int split = plan.split_k, grid = plan.num_ctas;
@@ -293,6 +295,7 @@ static w4a16_status_t run_gemm(const GemmCall& c, const DeviceFacts& dev, cudaSt
   a.K = c.W->K;
   a.n_tiles = c.W->N / kTileRows;
   a.n_kb = n_kb;
+  fast_divisor(static_cast<uint32_t>(a.n_tiles), &a.nt_magic, &a.nt_shift);
   a.paired = paired ? 1 : 0;
   a.nvfp4 = (c.W->flags & W4A16_PACK_NVFP4) ? 1 : 0;
   a.sorted_ids = R->sorted_ids;

@@ -81,14 +81,29 @@ struct Unit {
   bool ok;  // the block names a valid expert
 };
 
-__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int split_k, int64_t u) {
+// Unit u -> (block, tile, split).  Every role decodes every unit, so the divisions are 32-bit
+// (the host keeps unit counts below 2^31) and the one by n_tiles uses a precomputed
+// multiply-shift: q = (umulhi(n, m) + n) >> s with m = ceil(2^(32+s) / d) - 2^32 and
+// s = ceil(log2 d), exact for n < 2^31 (round-up reciprocal method).
+__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int split_k, int64_t u64) {
+  const uint32_t u = static_cast<uint32_t>(u64);
   Unit t;
-  t.split = static_cast<int>(u % split_k);
-  t.tile = u / split_k;
-  t.jt = static_cast<int>(t.tile % a.n_tiles);
-  t.b = static_cast<int>(t.tile / a.n_tiles);
-  t.kb0 = t.split * a.n_kb / split_k;
-  t.kb1 = (t.split + 1) * a.n_kb / split_k;
+  uint32_t tile;
+  if (split_k == 1) {
+    tile = u;
+    t.split = 0;
+    t.kb0 = 0;
+    t.kb1 = a.n_kb;
+  } else {
+    tile = u / static_cast<uint32_t>(split_k);
+    t.split = static_cast<int>(u - tile * static_cast<uint32_t>(split_k));
+    t.kb0 = t.split * a.n_kb / split_k;
+    t.kb1 = (t.split + 1) * a.n_kb / split_k;
+  }
+  const uint32_t b = (__umulhi(tile, a.nt_magic) + tile) >> a.nt_shift;
+  t.tile = tile;
+  t.b = static_cast<int>(b);
+  t.jt = static_cast<int>(tile - b * static_cast<uint32_t>(a.n_tiles));
   t.e = __ldg(a.expert_ids + t.b);
   t.ok = t.e >= 0 && t.e < a.E;
   return t;

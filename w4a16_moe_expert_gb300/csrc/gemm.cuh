@@ -15,6 +15,7 @@ struct GemmArgs {
   int a_sorted;
   const uint8_t* wblob;
   int E, N, K, n_tiles, n_kb;
+  uint32_t nt_magic, nt_shift;  // division by n_tiles: (umulhi(n, magic) + n) >> shift
   int paired;
   int nvfp4;  // the blob holds NVFP4 (E2M1 + E4M3 per 16) weights instead of INT4
   const int32_t* sorted_ids;
@@ -40,6 +41,15 @@ struct GemmArgs {
 };
 
 cudaError_t launch_gemm(GemmArgs& args, int grid, bool pdl, cudaStream_t stream);
+
+// Multiply-shift constants for dividing 31-bit numerators by d >= 1 (round-up reciprocal).
+inline void fast_divisor(uint32_t d, uint32_t* magic, uint32_t* shift) {
+  uint32_t l = 0;
+  while ((uint64_t(1) << l) < d) ++l;
+  const uint64_t m = ((uint64_t(1) << (32 + l)) + d - 1) / d - (uint64_t(1) << 32);
+  *magic = static_cast<uint32_t>(m);
+  *shift = l;
+}
 void plan_gemm(int total_slots, int E, int N, int K, int block_m, int rows_per_expert,
                int num_sms, w4a16_plan_t* plan);
 
