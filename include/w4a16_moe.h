@@ -99,12 +99,16 @@ w4a16_status_t w4a16_moe_align(const int32_t* topk_ids, int T, int top_k, int E,
  *          GEMM calls take.  Requires group == 32, K % 64 == 0, N % 128 == 0.
  * Layout of the tile stream: for expert e, 128-row tile j, 64-wide K block kb, one 4608-byte
  * chunk (codes of 128 rows x 64 K, nibble-interleaved for pairwise BF16 conversion, then the
- * 128 x 2 scales); chunks of one (e, j) are contiguous along K.
+ * 128 x 2 scales); chunks of one (e, j) are contiguous along K.  After the chunks, one mode
+ * byte per (e, j), padded to 16 bytes: a tile whose scales all lie in (0, 2^-5) stores them
+ * as s * 2^133 and is converted with one fused multiply-add per pair of weights; any other
+ * tile keeps its scales and the subtract-then-multiply conversion.  Both give the same BF16
+ * weight, bf16_rne((q - 8) * s).
  * ---------------------------------------------------------------------------------------- */
 #define W4A16_PACK_GATE_UP_PAIRED 0x1u
 #define W4A16_PACK_NVFP4 0x2u /* set by w4a16_pack_weights_nvfp4: the blob holds NVFP4 weights */
 #define W4A16_PACK_MAGIC 0x3631413457454f4dull /* "MOEW4A16" in little-endian bytes */
-#define W4A16_PACK_VERSION 1u
+#define W4A16_PACK_VERSION 2u
 
 typedef struct {
   uint64_t magic;   /* W4A16_PACK_MAGIC once filled */

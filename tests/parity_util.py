@@ -52,3 +52,11 @@ def sample_tokens(T: int, n: int, seed: int = 0) -> np.ndarray:
     if T <= n:
         return np.arange(T)
     return np.sort(rng.choice(T, size=n, replace=False))
+
+
+def tile_modes(W) -> torch.Tensor:
+    """The packed blob's mode byte per (expert, 128-row tile): 1 = scales stored times 2^133
+    (multiply-add conversion), 0 = scales as given (subtract-then-multiply conversion)."""
+    n_tiles, n_kb = W.N // 128, W.K // 64
+    off = 256 + W.E * n_tiles * n_kb * 4608
+    return W.blob[off:off + W.E * n_tiles].cpu().reshape(W.E, n_tiles)

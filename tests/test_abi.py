@@ -49,7 +49,9 @@ def test_status_strings(L):
 def test_sizes_and_capacity(L):
     assert lib.align_capacity(16, 2, 8, 16) == 32 + 8 * 15 + (16 - (32 + 8 * 15) % 16) % 16
     assert lib.align_capacity(3, 2, 3, 2) == 10
-    assert lib.packed_bytes(8, 512, 256) == 256 + 8 * 4 * 4 * 4608
+    # header, 4608-byte chunks, then one mode byte per (expert, tile) padded to 16 bytes
+    assert lib.packed_bytes(8, 512, 256) == 256 + 8 * 4 * 4 * 4608 + 32
+    assert lib.packed_bytes(3, 128, 64) == 256 + 3 * 4608 + 16
     assert lib.packed_bytes(8, 500, 256) == 0  # N % 128 != 0 is unsupported
     assert L.w4a16_packed_bytes(1, 128, 64, 64, 0) == 0  # group must be 32
     assert lib.gemm_workspace_size(64, 128, 1536, 2048, 16) > 16 << 20

@@ -37,7 +37,7 @@ PACK_GATE_UP_PAIRED = 0x1
 PACK_NVFP4 = 0x2
 LAYER_FUSED_TOPK = 0x1
 PACK_MAGIC = 0x3631413457454F4D
-PACK_VERSION = 1
+PACK_VERSION = 2
 
 DEVERR_BAD_EXPERT_ID = 0x1
 DEVERR_CAPACITY = 0x2

@@ -31,7 +31,7 @@ cudaError_t launch_pack_nvfp4(const uint8_t* codes, const uint8_t* scales, int E
                               uint32_t flags, void* packed, cudaStream_t stream);
 cudaError_t launch_pack(const int32_t* qweight, const uint16_t* scales, int E, int N, int K,
                         uint32_t flags, void* packed, cudaStream_t stream);
-cudaError_t launch_debug_dequant(const void* packed, int e, int N, int K, uint32_t flags,
+cudaError_t launch_debug_dequant(const void* packed, int E, int e, int N, int K, uint32_t flags,
                                  uint16_t* out, cudaStream_t stream);
 
 
@@ -104,6 +104,8 @@ static w4a16_status_t check_packed(const w4a16_packed_weights_t* W) {
     return fail(W4A16_BAD_PACKED_WEIGHT, "packed weight descriptor has unknown flags");
   if (reinterpret_cast<uintptr_t>(W->data) % 256)
     return fail(W4A16_BAD_PACKED_WEIGHT, "packed weight blob must be 256-byte aligned");
+  if (W->bytes != w4a16_packed_bytes(W->E, W->N, W->K, W->group, W->flags))
+    return fail(W4A16_BAD_PACKED_WEIGHT, "packed weight descriptor has a bad blob size");
   return W4A16_OK;
 }
 
@@ -298,6 +300,7 @@ static w4a16_status_t run_gemm(const GemmCall& c, const DeviceFacts& dev, cudaSt
   fast_divisor(static_cast<uint32_t>(a.n_tiles), &a.nt_magic, &a.nt_shift);
   a.paired = paired ? 1 : 0;
   a.nvfp4 = (c.W->flags & W4A16_PACK_NVFP4) ? 1 : 0;
+  a.tile_mode = a.wblob + tile_mode_offset(a.E, a.n_tiles, n_kb);
   a.sorted_ids = R->sorted_ids;
   a.expert_ids = R->expert_ids;
   a.ntp = R->num_tokens_padded;
@@ -377,7 +380,8 @@ w4a16_status_t w4a16_moe_align(const int32_t* topk_ids, int T, int top_k, int E,
 size_t w4a16_packed_bytes(int E, int N, int K, int group, uint32_t flags) {
   const int want = (flags & W4A16_PACK_NVFP4) ? 16 : 32;
   if (E < 0 || N <= 0 || K <= 0 || group != want || K % kBlockK || N % kTileRows) return 0;
-  return kHeaderBytes + static_cast<size_t>(E) * (N / kTileRows) * (K / kBlockK) * kChunkBytes;
+  const size_t modes = (static_cast<size_t>(E) * (N / kTileRows) + 15) / 16 * 16;
+  return static_cast<size_t>(tile_mode_offset(E, N / kTileRows, K / kBlockK)) + modes;
 }
 
 w4a16_status_t w4a16_pack_weights(const int32_t* qweight, const uint16_t* scales, int E, int N,
@@ -787,7 +791,7 @@ w4a16_status_t w4a16_debug_dequant(const w4a16_packed_weights_t* W, int expert, 
   if (expert < 0 || expert >= W->E || !out) return fail(W4A16_INVALID_ARG, "bad expert or output");
   DeviceFacts dev;
   if ((st = device_facts(&dev)) != W4A16_OK) return st;
-  cudaError_t err = launch_debug_dequant(W->data, expert, W->N, W->K, W->flags, out, stream);
+  cudaError_t err = launch_debug_dequant(W->data, W->E, expert, W->N, W->K, W->flags, out, stream);
   if (err != cudaSuccess) return cuda_fail(err, "debug_dequant launch");
   return W4A16_OK;
 }

@@ -20,6 +20,24 @@ constexpr int kScaleOffset = 2 * kCodeHalfBytes;         // 4096
 constexpr int kChunkBytes = kScaleOffset + kTileRows * 4;  // 4608 bytes per (tile, kb)
 constexpr int kHeaderBytes = 256;
 
+// After the chunks, one mode byte per (expert, tile): kTileScaled when every scale of the tile
+// lies in (0, 2^-5) and the chunks hold each scale as s * 2^133 (the multiply-add conversion),
+// kTilePlain otherwise (scales as given, the subtract-then-multiply conversion).
+constexpr uint8_t kTilePlain = 0, kTileScaled = 1;
+constexpr uint16_t kScaledMaxBits = 0x3CFF;  // largest BF16 s with s * 2^133 finite (< 2^-5)
+__host__ __device__ inline int64_t tile_mode_offset(int E, int n_tiles, int n_kb) {
+  return kHeaderBytes + static_cast<int64_t>(E) * n_tiles * n_kb * kChunkBytes;
+}
+
+// BF16 bits of s * 2^133 for 0 < s < 2^-5 (bits 0x0001..0x3CFF): exact, since a power-of-two
+// factor only moves the exponent (a subnormal s = m * 2^-133 becomes the integer m).
+__host__ __device__ inline uint16_t scale_times_2p133(uint16_t s) {
+  if (s >= 0x0080u) return static_cast<uint16_t>(s + (133u << 7));
+  int p = 6;  // subnormal: value m = s (1..127); normalise its leading bit
+  while (!((s >> p) & 1u)) --p;
+  return static_cast<uint16_t>(((127u + p) << 7) | ((static_cast<uint32_t>(s) << (7 - p)) & 0x7Fu));
+}
+
 // Device header at the start of every packed blob.
 struct PackedHeader {
   uint64_t magic;
@@ -80,6 +98,47 @@ __device__ __forceinline__ void dequant_word(uint32_t word, uint32_t scale2, uin
   out[1] = dequant_pair(word >> 4, scale2);
   out[2] = dequant_pair(word >> 8, scale2);
   out[3] = dequant_pair(word >> 12, scale2);
+}
+
+// Scaled tiles: the conversion without the subtraction.  Masked in place, a nibble at bits 0-3
+// of a BF16 half is the subnormal q * 2^-133, and at bits 4-7 it is q * 2^-129 (bit patterns
+// below 0x100 are linear in value across the subnormal/normal boundary).  With the chunk's
+// scale taken as s * 2^133 (and s * 2^129), one fused multiply-add with -8s forms (q - 8) * s
+// exactly before its single round-to-nearest-even, so the BF16 result equals the
+// subtract-then-scale definition (for s > 0; zero results are +0 as there).
+__device__ __forceinline__ uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+__device__ __forceinline__ void dequant_word_scaled(uint32_t word, uint32_t s133, uint32_t s129,
+                                                    uint32_t neg8s, uint32_t* out) {
+  out[0] = fma_bf16x2(word & 0x000F000Fu, s133, neg8s);
+  out[1] = fma_bf16x2(word & 0x00F000F0u, s129, neg8s);
+  const uint32_t w8 = word >> 8;
+  out[2] = fma_bf16x2(w8 & 0x000F000Fu, s133, neg8s);
+  out[3] = fma_bf16x2(w8 & 0x00F000F0u, s129, neg8s);
+}
+
+// Same output as dequant_row64 for a chunk of a scaled tile (scales2x = the two groups'
+// s * 2^133).
+__device__ __forceinline__ void dequant_row64_scaled(uint4 lo, uint4 hi, uint32_t scales2x,
+                                                     uint32_t (&r)[32]) {
+  uint32_t s129, neg8s;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(s129) : "r"(scales2x), "r"(0x3D803D80u));  // x 2^-4
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(neg8s) : "r"(s129), "r"(0x80808080u));     // x -2^-126
+  const uint32_t a0 = __byte_perm(scales2x, 0, 0x1010), a1 = __byte_perm(scales2x, 0, 0x3232);
+  const uint32_t b0 = __byte_perm(s129, 0, 0x1010), b1 = __byte_perm(s129, 0, 0x3232);
+  const uint32_t c0 = __byte_perm(neg8s, 0, 0x1010), c1 = __byte_perm(neg8s, 0, 0x3232);
+  dequant_word_scaled(lo.x, a0, b0, c0, &r[0]);
+  dequant_word_scaled(lo.y, a0, b0, c0, &r[4]);
+  dequant_word_scaled(lo.z, a0, b0, c0, &r[8]);
+  dequant_word_scaled(lo.w, a0, b0, c0, &r[12]);
+  dequant_word_scaled(hi.x, a1, b1, c1, &r[16]);
+  dequant_word_scaled(hi.y, a1, b1, c1, &r[20]);
+  dequant_word_scaled(hi.z, a1, b1, c1, &r[24]);
+  dequant_word_scaled(hi.w, a1, b1, c1, &r[28]);
 }
 
 // Dequantise one tile row of a 64-wide K block from a chunk (shared or global memory):

@@ -21,7 +21,9 @@
 //     Weights and activations complete on separate mbarriers, so a dependent launch streams
 //     and dequantises its first weights before its inputs exist;
 //   * warps 8-15 (two dequant warpgroups, alternating stages) turn codes into BF16 pairs and
-//     store them to TMEM with tcgen05.st; warp 1 issues tcgen05.mma from one elected lane;
+//     store them to TMEM with tcgen05.st (one fused multiply-add per pair for tiles whose
+//     scales the packer stored pre-multiplied by 2^133, else subtract then multiply);
+//     warp 1 issues tcgen05.mma from one elected lane;
 //     warps 4-7 drain the double-buffered accumulator with tcgen05.ld and write the results;
 //   * a persistent grid walks (block, 128-row tile, K split) units found from
 //     num_tokens_padded on the device (no host read-back); K splits (decode) write FP32
@@ -547,6 +549,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
       const Unit un = decode_unit(a, split_k, u);
       if (!un.ok) continue;
+      // the tile's INT4 conversion (uniform over the unit, read while the weights are in flight)
+      const bool scaled =
+          __ldg(a.tile_mode + static_cast<int64_t>(un.e) * a.n_tiles + un.jt) == kTileScaled;
       for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
         if (it % kDqGroups != static_cast<uint32_t>(g)) continue;
         const int nsub = min(KS, un.kb1 - kb);
@@ -579,6 +584,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (sb < nsub) {
               uint32_t v[32];
               dequant_row64_nvfp4(lo[sb], hi[sb], s2[sb], v);
+              tmem_st32(lane_base + sa * (KS * 32) + sb * 32, v);
+            }
+          }
+        } else if (scaled) {
+#pragma unroll
+          for (int sb = 0; sb < KS; ++sb) {
+            if (sb < nsub) {
+              uint32_t v[32];
+              dequant_row64_scaled(lo[sb], hi[sb], s2[sb], v);
               tmem_st32(lane_base + sa * (KS * 32) + sb * 32, v);
             }
           }

@@ -18,6 +18,7 @@ struct GemmArgs {
   uint32_t nt_magic, nt_shift;  // division by n_tiles: (umulhi(n, magic) + n) >> shift
   int paired;
   int nvfp4;  // the blob holds NVFP4 (E2M1 + E4M3 per 16) weights instead of INT4
+  const uint8_t* tile_mode;  // [E * n_tiles] kTilePlain / kTileScaled (INT4 conversion of a tile)
   const int32_t* sorted_ids;
   const int32_t* expert_ids;
   const int32_t* ntp;
