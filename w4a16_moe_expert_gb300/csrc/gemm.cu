@@ -40,7 +40,7 @@ constexpr int kDqGroups = 2;  // dequant warpgroups; stage it goes to group it %
 constexpr int kGemmThreads = 256 + 128 * kDqGroups;
 constexpr int kTmemCols = 512;
 constexpr int kSmemBudget = 216 * 1024;
-constexpr int kEpiStageBytes = 16 * 32 * 4;  // per epilogue warp: 16 tokens x 32 rows x 4 B
+constexpr int kEpiStageBytes = 16 * 36 * 4;  // per epilogue warp: 16 tokens x (32 + 4 pad) x 4 B
 constexpr int kGatherThreads = 64;  // warps 2 and 3 gather activation rows with cp.async
 
 // NT = block_m = MMA N; KS = 64-wide K sub-blocks per pipeline stage (one weight copy of
@@ -172,13 +172,15 @@ __device__ __forceinline__ void store_chunk16(const GemmArgs& a, const Unit& un,
       *reinterpret_cast<uint4*>(a.C + row * a.ldc + col) = v;
     }
   } else {
-    float* st = reinterpret_cast<float*>(stage);  // [16 tokens][32 rows]
+    // [16 tokens][36]: rows padded by 16 bytes so that the 16-byte reads below (lanes 2t and
+    // 2t + 1 read token t) fall on distinct banks within each quarter warp
+    float* st = reinterpret_cast<float*>(stage);
 #pragma unroll
-    for (int jj = 0; jj < 16; ++jj) st[jj * 32 + lane] = __uint_as_float(r[jj]);
+    for (int jj = 0; jj < 16; ++jj) st[jj * 36 + lane] = __uint_as_float(r[jj]);
     __syncwarp();
     if (row >= 0) {
       const int col = tile_row_to_canonical(un.jt, 32 * q + 16 * half, a.N, a.paired != 0);
-      const float4* src = reinterpret_cast<const float4*>(st + tok * 32 + 16 * half);
+      const float4* src = reinterpret_cast<const float4*>(st + tok * 36 + 16 * half);
       if (a.merge_w) {
         // top-k merge: this slot's weighted row is added into its token's FP32 row
         if (routed) {
