@@ -385,6 +385,19 @@ def run_ours(args, rank, world, local_rank):
             ts.append(e0.elapsed_time(e1) * 1e3 / n)
         return statistics.median(ts)
 
+    # device time of the layer call (inputs resident), per call like the projections: a graph
+    # of back-to-back calls over rotating weight copies; as specified, with the top-k merge
+    # fused into the down GEMM, and as one fused GEMM kernel
+    layer_us, fused_us, one_us = [], [], []
+    for c in cases:
+        for mode, dst in ((0, layer_us), (1, fused_us), (2, one_us)):
+            dst.append(per_call_us(
+                lambda i: lib.moe_layer(c["x"], w13s[i % c["n_gu"]], w2s[i % c["n_dn"]], c["ids"], c["w"],
+                                        E_global=wl.E_global, block_m=c["block_m"], out=c["out"],
+                                        workspace=c["layer_ws"], fused_topk=mode == 1,
+                                        fused=mode == 2),
+                max(c["R_gu"], c["R_dn"])))
+
     extras = {}
     if not args.no_extras:
         from w4a16_moe_expert_gb300.workloads import draw_nvfp4_weights
@@ -481,25 +494,6 @@ def run_ours(args, rank, world, local_rank):
     e2e_us = [statistics.fmean(evs[i][0].elapsed_time(evs[i][1]) * 1e3 for evs in e2e_events)
               for i in range(len(cases))]
 
-    # device time of the layer call alone (inputs resident, after an L2 flush), as specified
-    # and with the top-k merge fused into the down GEMM
-    layer_us, fused_us = [], []
-    for c in cases:
-        for fused, dst in ((False, layer_us), (True, fused_us)):
-            ts = []
-            for s in range(args.warmup + min(args.steps, 20)):
-                flush.zero_()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-                lib.moe_layer(c["x"], w13, w2, c["ids"], c["w"], E_global=wl.E_global,
-                              block_m=c["block_m"], out=c["out"], workspace=c["layer_ws"],
-                              fused_topk=fused)
-                e1.record()
-                if s >= args.warmup:
-                    ts.append((e0, e1))
-            torch.cuda.synchronize()
-            dst.append(statistics.median(a.elapsed_time(b) * 1e3 for a, b in ts))
-
     # aggregate metric and roofline
     w_bytes = sum(c["acct"]["gate_up"]["weight_bytes"] + c["acct"]["down"]["weight_bytes"] for c in cases)
     gemm_us = sum(g + d for g, d in call_us)
@@ -541,7 +535,7 @@ def run_ours(args, rank, world, local_rank):
     }
 
     sweep = []
-    for c, u, cu, e, ly, fz in zip(cases, stage_us, call_us, e2e_us, layer_us, fused_us):
+    for c, u, cu, e, ly, fz, one in zip(cases, stage_us, call_us, e2e_us, layer_us, fused_us, one_us):
         a = c["acct"]
         row = {"T": c["T"], "T_r": a["T_r"], "E_act": a["E_act"], "block_m": c["block_m"],
                "gate_up_us": round(cu[0], 2), "down_us": round(cu[1], 2),
@@ -551,7 +545,8 @@ def run_ours(args, rank, world, local_rank):
                                   "down": round(u[2], 2), "topk_sum": round(u[3], 2)},
                "layer_e2e_us": round(e, 2),
                "layer_us": round(ly, 2),
-               "layer_fused_topk_us": round(fz, 2)}
+               "layer_fused_topk_us": round(fz, 2),
+               "layer_one_kernel_us": round(one, 2)}
         for name, t_us in (("gate_up", cu[0]), ("down", cu[1])):
             d = a[name]
             roof_us = max(d["bytes"] / (hbm * 1e9), d["flops"] / (tflops_peak * 1e12)) * 1e6

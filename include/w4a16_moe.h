@@ -304,6 +304,16 @@ w4a16_status_t w4a16_topk_sum(const float* Y, const int32_t* topk_ids,
  * tolerance but not bitwise reproducible; without the flag the sum runs over slots in order
  * and is reproducible. */
 #define W4A16_LAYER_FUSED_TOPK 0x1u
+/* W4A16_LAYER_FUSED: gate_up and down run as ONE persistent kernel (the single-kernel layer
+ * of the humans& page's "Dedicated warps keep the pipeline busy", here without token
+ * dispatch), with the top-k merge of W4A16_LAYER_FUSED_TOPK in its down epilogue.  Units of
+ * the down GEMM follow the gate_up units in every CTA's sequence; a down unit's activation
+ * loads wait until all gate_up tiles of its block are stored (a per-block counter in the
+ * workspace, bounded wait), while its weights stream from the start, so the down projection
+ * overlaps the gate_up tail.  The launch is cooperative (all CTAs resident); a wait that runs
+ * out sets W4A16_DEVERR_TIMEOUT.  Kernels: align, (row gather for block_m >= 64), zeroing, the
+ * fused GEMM, rounding.  Not bitwise reproducible, as for W4A16_LAYER_FUSED_TOPK; implies it. */
+#define W4A16_LAYER_FUSED 0x2u
 int w4a16_plan_block_m(int T, int top_k, int E, int E_global);
 size_t w4a16_layer_workspace_size(int T, int top_k, int E, int E_global, int H, int I,
                                   int block_m);

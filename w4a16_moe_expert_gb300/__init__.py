@@ -36,6 +36,7 @@ C_FP32 = 0x4
 PACK_GATE_UP_PAIRED = 0x1
 PACK_NVFP4 = 0x2
 LAYER_FUSED_TOPK = 0x1
+LAYER_FUSED = 0x2
 PACK_MAGIC = 0x3631413457454F4D
 PACK_VERSION = 2
 
@@ -438,9 +439,11 @@ def layer_workspace_size(T: int, top_k: int, E: int, H: int, I: int, E_global: i
 def moe_layer(x: torch.Tensor, w13: PackedWeights, w2: PackedWeights, topk_ids: torch.Tensor,
               topk_weights: torch.Tensor, E_global: int = 0, block_m: int = 0,
               out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-              dev_err: Optional[torch.Tensor] = None, fused_topk: bool = False) -> torch.Tensor:
+              dev_err: Optional[torch.Tensor] = None, fused_topk: bool = False,
+              fused: bool = False) -> torch.Tensor:
     """The whole layer; ``fused_topk`` merges the top-k outputs inside the down GEMM
-    (atomic FP32 sums: within the tolerance, not bitwise reproducible)."""
+    (atomic FP32 sums: within the tolerance, not bitwise reproducible); ``fused`` also runs
+    gate_up and down as one persistent kernel (and implies ``fused_topk``)."""
     _cuda(x, torch.bfloat16, "x")
     _cuda(topk_ids, torch.int32, "topk_ids")
     _cuda(topk_weights, torch.float32, "topk_weights")
@@ -453,7 +456,8 @@ def moe_layer(x: torch.Tensor, w13: PackedWeights, w2: PackedWeights, topk_ids: 
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
     _check("w4a16_moe_layer_ex", load().w4a16_moe_layer_ex(
         _ptr(x), ctypes.byref(w13.desc), ctypes.byref(w2.desc), _ptr(topk_ids), _ptr(topk_weights),
-        T, k, E_global, block_m, LAYER_FUSED_TOPK if fused_topk else 0, _ptr(out), _ptr(workspace),
+        T, k, E_global, block_m, (LAYER_FUSED if fused else 0) | (LAYER_FUSED_TOPK if fused_topk else 0),
+        _ptr(out), _ptr(workspace),
         workspace.numel(), _ptr(dev_err), _stream()))
     return out
 

@@ -202,6 +202,25 @@ static void pdl_config(int64_t work_items, int num_sms, cudaStream_t stream, cud
   cfg->numAttrs = 1;
 }
 
+// Zeroes n floats at p and m 32-bit words at q (both 16-byte aligned, n and m multiples of 4).
+__global__ void __launch_bounds__(256)
+    zero2_kernel(float* __restrict__ p, int64_t n4, int32_t* __restrict__ q, int64_t m4) {
+  pdl_wait();  // the previous call's last kernel may still read these buffers
+  pdl_launch_dependents();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (int64_t i = i0; i < n4; i += stride) reinterpret_cast<float4*>(p)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t i = i0; i < m4; i += stride) reinterpret_cast<int4*>(q)[i] = make_int4(0, 0, 0, 0);
+}
+
+static cudaError_t launch_zero2(float* p, int64_t n, int32_t* q, int64_t m, int num_sms,
+                                cudaStream_t stream) {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  pdl_config(std::max(n, m) / 4, num_sms, stream, &cfg, attr);
+  return cudaLaunchKernelEx(&cfg, zero2_kernel, p, n / 4, q, m / 4);
+}
+
 static cudaError_t launch_zero_f32(float* p, int64_t n, int num_sms, cudaStream_t stream) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
@@ -238,7 +257,11 @@ struct GemmCall {
   int merge_k = 0;
 };
 
-static w4a16_status_t run_gemm(const GemmCall& c, const DeviceFacts& dev, cudaStream_t stream) {
+// Checks a GEMM call and fills the kernel arguments and grid; *empty is set when there is
+// nothing to compute (no capacity or no experts).
+static w4a16_status_t prepare_gemm(const GemmCall& c, const DeviceFacts& dev, GemmArgs* out,
+                                   int* out_grid, bool* empty) {
+  *empty = false;
   w4a16_status_t st = check_packed(c.W);
   if (st != W4A16_OK) return st;
   const w4a16_routing_t* R = c.R;
@@ -267,7 +290,10 @@ static w4a16_status_t run_gemm(const GemmCall& c, const DeviceFacts& dev, cudaSt
     return fail(W4A16_INVALID_ARG, "C must be 16-byte aligned with 16-byte aligned rows");
   if ((c.row_flags & W4A16_C_FP32) && c.epilogue != W4A16_EPILOGUE_NONE)
     return fail(W4A16_INVALID_ARG, "FP32 output is available with epilogue NONE only");
-  if (R->capacity == 0 || c.W->E == 0) return W4A16_OK;
+  if (R->capacity == 0 || c.W->E == 0) {
+    *empty = true;
+    return W4A16_OK;
+  }
 
   if ((R->capacity / R->block_m) * static_cast<int64_t>(c.W->N / kTileRows) * 16 >= (int64_t(1) << 31))
     return fail(W4A16_UNSUPPORTED, "routing capacity too large for one call (units must stay below 2^31)");
@@ -285,7 +311,7 @@ static w4a16_status_t run_gemm(const GemmCall& c, const DeviceFacts& dev, cudaSt
   if (split > 1 && (!c.ws || c.ws_bytes < cnt_bytes + kPartialBytes))
     return fail(W4A16_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes", cnt_bytes + kPartialBytes);
 
-  GemmArgs a;
+  GemmArgs& a = *out;
   std::memset(&a, 0, sizeof a);
   a.A = c.A;
   a.lda = c.lda;
@@ -322,6 +348,16 @@ static w4a16_status_t run_gemm(const GemmCall& c, const DeviceFacts& dev, cudaSt
   a.routing_ready = c.routing_ready;
   a.merge_w = c.merge_w;
   a.merge_k = c.merge_k;
+  *out_grid = grid;
+  return W4A16_OK;
+}
+
+static w4a16_status_t run_gemm(const GemmCall& c, const DeviceFacts& dev, cudaStream_t stream) {
+  GemmArgs a;
+  int grid = 0;
+  bool empty = false;
+  w4a16_status_t st = prepare_gemm(c, dev, &a, &grid, &empty);
+  if (st != W4A16_OK || empty) return st;
   cudaError_t err = launch_gemm(a, grid, true, stream);
   if (err != cudaSuccess) return cuda_fail(err, "moe_gemm launch");
   return W4A16_OK;
@@ -654,7 +690,7 @@ w4a16_status_t w4a16_plan_gemm(int total_slots, int E, int N, int K, int block_m
 struct LayerLayout {
   int block_m;
   int64_t cap;
-  size_t off_sorted, off_expert, off_ntp, off_cnt, off_part, off_xs, off_h, off_y, total;
+  size_t off_sorted, off_expert, off_ntp, off_cnt, off_part, off_xs, off_h, off_y, off_done, total;
 };
 
 static LayerLayout layer_layout(int T, int top_k, int E, int E_global, int H, int I, int block_m) {
@@ -678,6 +714,8 @@ static LayerLayout layer_layout(int T, int top_k, int E, int E_global, int H, in
   o = round_up(o + static_cast<size_t>(L.cap) * I * 2, 256);
   L.off_y = o;
   o = round_up(o + static_cast<size_t>(T) * top_k * H * 4, 256);
+  L.off_done = o;  // fused layer: finished gate_up tiles per block (multiple of 4 words)
+  o = round_up(o + round_up(static_cast<size_t>(L.cap / L.block_m), 4) * 4, 256);
   L.total = o;
   return L;
 }
@@ -704,8 +742,10 @@ w4a16_status_t w4a16_moe_layer_ex(const uint16_t* x, const w4a16_packed_weights_
                                   int block_m, uint32_t layer_flags, uint16_t* out,
                                   void* workspace, size_t workspace_bytes, int32_t* dev_err,
                                   w4a16_stream_t stream) {
-  if (layer_flags & ~W4A16_LAYER_FUSED_TOPK) return fail(W4A16_INVALID_ARG, "unknown layer flags");
-  const bool fused = (layer_flags & W4A16_LAYER_FUSED_TOPK) != 0;
+  if (layer_flags & ~(W4A16_LAYER_FUSED_TOPK | W4A16_LAYER_FUSED))
+    return fail(W4A16_INVALID_ARG, "unknown layer flags");
+  const bool one_kernel = (layer_flags & W4A16_LAYER_FUSED) != 0;
+  const bool fused = one_kernel || (layer_flags & W4A16_LAYER_FUSED_TOPK) != 0;
   w4a16_status_t st = check_packed(w13);
   if (st != W4A16_OK) return st;
   if ((st = check_packed(w2)) != W4A16_OK) return st;
@@ -743,7 +783,13 @@ w4a16_status_t w4a16_moe_layer_ex(const uint16_t* x, const w4a16_packed_weights_
                                      reinterpret_cast<int32_t*>(ws + L.off_cnt),
                                      static_cast<int>(split_unit_budget(L.block_m)), stream);
   if (err != cudaSuccess) return cuda_fail(err, "moe_align launch");
-  if (fused) {  // the down GEMM adds into FP32 token sums held where the per-slot rows would be
+  int32_t* blk_done = reinterpret_cast<int32_t*>(ws + L.off_done);
+  if (one_kernel) {  // FP32 token sums and the per-block gate_up completion counts
+    err = launch_zero2(y, static_cast<int64_t>(T) * H, blk_done,
+                       static_cast<int64_t>(round_up(static_cast<size_t>(L.cap / L.block_m), 4)),
+                       dev.num_sms, stream);
+    if (err != cudaSuccess) return cuda_fail(err, "zero launch");
+  } else if (fused) {  // the down GEMM adds into FP32 token sums held where the per-slot rows would be
     err = launch_zero_f32(y, static_cast<int64_t>(T) * H, dev.num_sms, stream);
     if (err != cudaSuccess) return cuda_fail(err, "zero launch");
   }
@@ -764,10 +810,33 @@ w4a16_status_t w4a16_moe_layer_ex(const uint16_t* x, const w4a16_packed_weights_
               (pre_gather ? W4A16_A_ROWS_SORTED : 0u) | W4A16_C_ROWS_SORTED, h, I,
               ws + L.off_cnt, (L.off_xs - L.off_cnt), rows_hint, nullptr, dev_err,
               pre_gather ? 1 : 0};
-  if ((st = run_gemm(g1, dev, stream)) != W4A16_OK) return st;
   GemmCall g2{h, I, 1, w2, &R, W4A16_EPILOGUE_NONE, W4A16_A_ROWS_SORTED | W4A16_C_FP32,
               reinterpret_cast<uint16_t*>(y), H,
               ws + L.off_cnt, (L.off_xs - L.off_cnt), rows_hint, nullptr, dev_err, 1};
+  if (one_kernel) {
+    const w4a16_schedule_t one_split{1, 0};
+    g1.sched = &one_split;
+    g2.sched = &one_split;
+    g2.merge_w = topk_weights;
+    g2.merge_k = top_k;
+    GemmArgs a1, a2;
+    int grid1 = 0, grid2 = 0;
+    bool empty1 = false, empty2 = false;
+    if ((st = prepare_gemm(g1, dev, &a1, &grid1, &empty1)) != W4A16_OK) return st;
+    if ((st = prepare_gemm(g2, dev, &a2, &grid2, &empty2)) != W4A16_OK) return st;
+    if (!empty1 && !empty2) {
+      a1.signal_done = blk_done;
+      a2.wait_done = blk_done;
+      a2.wait_count = a1.n_tiles;
+      a2.routing_ready = a1.routing_ready;
+      err = launch_layer_fused(a1, a2, dev.num_sms, stream);
+      if (err != cudaSuccess) return cuda_fail(err, "fused layer launch");
+    }
+    err = launch_round_bf16(y, static_cast<int64_t>(T) * H, out, dev.num_sms, stream);
+    if (err != cudaSuccess) return cuda_fail(err, "round launch");
+    return W4A16_OK;
+  }
+  if ((st = run_gemm(g1, dev, stream)) != W4A16_OK) return st;
   if (fused) {
     const w4a16_schedule_t one_split{1, 0};  // the merge is the reduction: no K splits
     g2.sched = &one_split;

@@ -281,6 +281,31 @@ __device__ __forceinline__ bool mbar_wait_plain(uint32_t bar, uint32_t parity) {
   return true;
 }
 
+// Release increment of a counter in global memory (pairs with wait_count_at_least).
+__device__ __forceinline__ void red_release_add(int32_t* p, int32_t v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait until a counter in global memory reaches `want` (acquire: what was stored
+// before the increments is visible afterwards).  On timeout the CTA's abort flag and the
+// caller's error word are set.
+__device__ __forceinline__ bool wait_count_at_least(const int32_t* p, int32_t want,
+                                                    volatile int* abort_flag, int32_t* dev_err) {
+  const long long t0 = clock64();
+  while (true) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= want) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      set_dev_err(dev_err, W4A16_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+    __nanosleep(200);
+  }
+}
+
 // ---- bulk TMA and cp.async -------------------------------------------------------------------
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
@@ -315,6 +340,11 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
 }
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// generic-proxy writes to global memory (seen through an acquire) -> later async-proxy reads
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -79,6 +79,7 @@ struct GemmCfg {
 
 struct Unit {
   int b, jt, split, kb0, kb1, e;
+  int gi;  // which GEMM of a fused layer call (0: gate_up, 1: down); 0 otherwise
   int64_t tile;
   bool ok;  // the block names a valid expert
 };
@@ -108,11 +109,37 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int split_k, int6
   t.jt = static_cast<int>(tile - b * static_cast<uint32_t>(a.n_tiles));
   t.e = __ldg(a.expert_ids + t.b);
   t.ok = t.e >= 0 && t.e < a.E;
+  t.gi = 0;
   return t;
+}
+
+// Fused layer: units [0, units0) are the first GEMM's (gate_up), the rest the second's (down),
+// both over the same aligned blocks.  A plain call has one GEMM (a2 is a).
+template <bool FUSED>
+__device__ __forceinline__ Unit decode_any(const GemmArgs& a, const GemmArgs& a2, int split_k,
+                                           uint32_t units0, int64_t u64) {
+  if (!FUSED) return decode_unit(a, split_k, u64);
+  const uint32_t u = static_cast<uint32_t>(u64);
+  if (u < units0) return decode_unit(a, 1, u);
+  Unit t = decode_unit(a2, 1, u - units0);
+  t.gi = 1;
+  return t;
+}
+
+// The per-GEMM arguments of a unit.
+template <bool FUSED>
+__device__ __forceinline__ const GemmArgs& args_of(const GemmArgs& a, const GemmArgs& a2,
+                                                   const Unit& un) {
+  return (FUSED && un.gi) ? a2 : a;
 }
 
 __device__ __forceinline__ void named_bar_epi() {
   asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// the 64 threads of the activation warps (2 and 3)
+__device__ __forceinline__ void named_bar_act() {
+  asm volatile("bar.sync 2, 64;" ::: "memory");
 }
 
 // OR of `pred` over the 128 epilogue threads (they all take the same branch afterwards, which
@@ -215,9 +242,8 @@ __device__ __forceinline__ void store_chunk16(const GemmArgs& a, const Unit& un,
   __syncwarp();  // the staging area is reused by the next chunk
 }
 
-template <int NT, int KS>
-__global__ void __launch_bounds__(kGemmThreads, 1)
-    moe_gemm_kernel(const __grid_constant__ GemmArgs a) {
+template <int NT, int KS, bool FUSED>
+__device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2) {
   using Cfg = GemmCfg<NT, KS>;
   constexpr int S_W = Cfg::kWStages;
   constexpr int S_B = Cfg::kBStages;
@@ -250,6 +276,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool gather = !a.a_sorted;
+  // a fused call may mix gathered and TMA-loaded activations (one GEMM each): every stage then
+  // completes on 64 arrivals, the TMA path's lane 0 also expecting the tile's bytes
+  const bool any_tma = FUSED ? (a.a_sorted || a2.a_sorted) : a.a_sorted;
 
   if (tid == 0) {
     for (int s = 0; s < S_W; ++s) {
@@ -257,7 +286,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(smem_u32(&wempty[s]), 4);
     }
     for (int s = 0; s < S_B; ++s) {
-      mbar_init(smem_u32(&bfull[s]), gather ? kGatherThreads : 1);
+      mbar_init(smem_u32(&bfull[s]), (FUSED || gather) ? kGatherThreads : 1);
       mbar_init(smem_u32(&bempty[s]), 1);
     }
     for (int s = 0; s < S_A; ++s) {
@@ -275,7 +304,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     *b_issued = 0;
     fence_mbar_init();
   }
-  if (warp == 2 && lane == 0 && !gather) tma_prefetch_desc(&a.tmap_a);
+  if (warp == 2 && lane == 0) {
+    if (a.a_sorted) tma_prefetch_desc(&a.tmap_a);
+    if (FUSED && a2.a_sorted) tma_prefetch_desc(&a2.tmap_a);
+  }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -297,7 +329,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // Fewer K splits when the routed blocks would overflow the partial-sum scratch.
   int split_k = a.split_k;
   while (split_k > 1 && nblocks * a.n_tiles * split_k > a.max_split_units) --split_k;
-  const int64_t n_units = nblocks * a.n_tiles * split_k;
+  const int64_t units0 = nblocks * a.n_tiles * split_k;
+  const int64_t n_units = FUSED ? units0 + nblocks * a2.n_tiles : units0;
+  const uint32_t units0_u = static_cast<uint32_t>(units0);
 
   if (warp == 0) {
     // ---------------- weight producer: one bulk copy per stage, on a rotating lane ------------
@@ -307,10 +341,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint64_t policy = a.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
     uint32_t it = 0;
     for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-      const Unit un = decode_unit(a, split_k, u);
+      const Unit un = decode_any<FUSED>(a, a2, split_k, units0_u, u);
       if (!un.ok) continue;
-      const uint8_t* strip = a.wblob + kHeaderBytes +
-                             ((static_cast<int64_t>(un.e) * a.n_tiles + un.jt) * a.n_kb) * kChunkBytes;
+      const GemmArgs& g = args_of<FUSED>(a, a2, un);
+      const uint8_t* strip = g.wblob + kHeaderBytes +
+                             ((static_cast<int64_t>(un.e) * g.n_tiles + un.jt) * g.n_kb) * kChunkBytes;
       for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
         const int nsub = min(KS, un.kb1 - kb);
         const int s = it % S_W;
@@ -332,13 +367,81 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ---------------- activation producer ----------------
     pdl_wait();  // activations may be the previous kernel's output
     uint32_t it = 0;
-    if (gather) {
+    if constexpr (FUSED) {
+      // Per unit: gathered rows (cp.async, both warps) or sorted rows (TMA issued by warp 2);
+      // every stage completes on the 64 threads' arrivals.  Units of the second GEMM read rows
+      // that other CTAs' first-GEMM epilogues write during this launch: thread 0 waits for the
+      // block's completion count, then the async proxy is fenced before the tensor loads.
+      const int gt = tid - 64;
+      const int c = gt & 7;
+      constexpr int R = NT / 8;
+      for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
+        const Unit un = decode_any<FUSED>(a, a2, split_k, units0_u, u);
+        if (!un.ok) continue;
+        const GemmArgs& g = args_of<FUSED>(a, a2, un);
+        if (g.wait_done) {
+          if (gt == 0) wait_count_at_least(g.wait_done + un.b, g.wait_count, abort_flag, g.dev_err);
+          named_bar_act();
+          if (*abort_flag) goto fprod_done;
+          fence_proxy_async_global();
+        }
+        if (!g.a_sorted) {
+          int32_t arow[R];
+#pragma unroll
+          for (int j = 0; j < R; ++j) {
+            const int32_t i = __ldg(g.sorted_ids + static_cast<int64_t>(un.b) * g.block_m + (gt >> 3) + 8 * j);
+            arow[j] = (i >= 0 && i < g.total_slots) ? i / g.a_row_div : -1;
+          }
+          for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
+            const int nsub = min(KS, un.kb1 - kb);
+            const int s = it % S_B;
+            const uint32_t ph = (it / S_B) & 1;
+            if (!mbar_wait(smem_u32(&bempty[s]), ph ^ 1, abort_flag, g.dev_err)) goto fprod_done;
+            const uint32_t bdst = smem_u32(b_ring + s * Cfg::kBBytes);
+            for (int sb = 0; sb < nsub; ++sb) {
+#pragma unroll
+              for (int j = 0; j < R; ++j) {
+                if (arow[j] < 0) continue;
+                const int r = (gt >> 3) + 8 * j;
+                const uint32_t dst = bdst + sb * Cfg::kSubB + r * 128 + ((c ^ (r & 7)) << 4);
+                cp_async_16(dst, g.A + static_cast<int64_t>(arow[j]) * g.lda + (kb + sb) * kBlockK + c * 8, 16u);
+              }
+            }
+            cp_async_arrive_noinc(smem_u32(&bfull[s]));
+          }
+        } else {
+          for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
+            const int nsub = min(KS, un.kb1 - kb);
+            const int s = it % S_B;
+            const uint32_t ph = (it / S_B) & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bempty[s]), ph ^ 1, abort_flag, g.dev_err)))
+              goto fprod_done;
+            const uint32_t bb = smem_u32(&bfull[s]);
+            if (gt == 0)
+              mbar_arrive_expect_tx(bb, nsub * Cfg::kSubB);
+            else
+              mbar_arrive(bb);
+            if (warp == 2) {
+              __syncwarp();
+              for (int sb = 0; sb < nsub; ++sb)
+                if (lane == static_cast<int>((it * KS + sb) & 31))
+                  tma_load_2d(smem_u32(b_ring + s * Cfg::kBBytes + sb * Cfg::kSubB), &g.tmap_a,
+                              (kb + sb) * kBlockK, static_cast<int>(un.b * g.block_m), bb);
+              __syncwarp();
+            }
+          }
+        }
+      }
+    fprod_done:
+      cp_async_wait_all();
+      if (warp == 2 && lane == 0) *b_issued = it;
+    } else if (gather) {
       // rows gathered with 16-byte cp.async into the 128-byte-swizzled K-major layout
       const int g = tid - 64;
       const int c = g & 7;  // 16-byte chunk of a 128-byte row handled by this thread
       constexpr int R = NT / 8;  // rows per thread: (g >> 3) + 8j
       for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const Unit un = decode_unit(a, split_k, u);
+        const Unit un = decode_any<FUSED>(a, a2, split_k, units0_u, u);
         if (!un.ok) continue;
         int32_t arow[R];
 #pragma unroll
@@ -371,7 +474,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp == 2) {
       // rows already in sorted order: one 2-D TMA tile per K sub-block, rotating lanes
       for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const Unit un = decode_unit(a, split_k, u);
+        const Unit un = decode_any<FUSED>(a, a2, split_k, units0_u, u);
         if (!un.ok) continue;
         for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
           const int nsub = min(KS, un.kb1 - kb);
@@ -402,8 +505,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (elect_one()) {
       uint32_t it = 0, lu = 0;
       for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const Unit un = decode_unit(a, split_k, u);
+        const Unit un = decode_any<FUSED>(a, a2, split_k, units0_u, u);
         if (!un.ok) continue;
+        const bool rows_gathered = FUSED ? !args_of<FUSED>(a, a2, un).a_sorted : gather;
         const int ab = lu & 1;
         const uint32_t pab = (lu >> 1) & 1;
         if (!mbar_wait(smem_u32(&accempty[ab]), pab ^ 1, abort_flag, a.dev_err)) goto mma_done;
@@ -417,7 +521,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t pa = (it / S_A) & 1;
           if (!mbar_wait(smem_u32(&afull[sa]), pa, abort_flag, a.dev_err)) goto mma_done;
           if (!mbar_wait(smem_u32(&bfull[sbi]), pb, abort_flag, a.dev_err)) goto mma_done;
-          if (gather) fence_proxy_async_smem();  // cp.async (generic proxy) rows -> tensor core
+          if (rows_gathered) fence_proxy_async_smem();  // cp.async (generic proxy) rows -> tensor core
           tc_fence_after();
           const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((sbi * Cfg::kBBytes) >> 4);
           const uint32_t a_tmem = tmem_base + Cfg::kACol0 + sa * (KS * 32);
@@ -461,8 +565,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint8_t* epi_stage = epi_stage_base + q * kEpiStageBytes;
     uint32_t lu = 0;
     for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-      const Unit un = decode_unit(a, split_k, u);
+      const Unit un = decode_any<FUSED>(a, a2, split_k, units0_u, u);
       if (!un.ok) continue;
+      const GemmArgs& g = args_of<FUSED>(a, a2, un);
       named_bar_epi();  // the previous unit's readers of epi_rows / last_flag are done
       if (t < NT) epi_rows[t] = __ldg(a.sorted_ids + static_cast<int64_t>(un.b) * a.block_m + t);
       named_bar_epi();
@@ -485,7 +590,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tc_fence_before();
             mbar_arrive(smem_u32(&accempty[ab]));
           }
-          store_chunk16(a, un, q, lane, c0, epi_rows, r0, epi_stage);
+          store_chunk16(g, un, q, lane, c0, epi_rows, r0, epi_stage);
           if (c0 + 16 < NT) {
             tmem_wait_ld16(r1);
             if (c0 + 32 < NT) tmem_ld16(taddr + c0 + 32, r0);
@@ -493,7 +598,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               tc_fence_before();
               mbar_arrive(smem_u32(&accempty[ab]));
             }
-            store_chunk16(a, un, q, lane, c0 + 16, epi_rows, r1, epi_stage);
+            store_chunk16(g, un, q, lane, c0 + 16, epi_rows, r1, epi_stage);
           }
         }
       } else {
@@ -534,10 +639,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t r[16];
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) r[jj] = __float_as_uint(v[jj]);
-            store_chunk16(a, un, q, lane, c0, epi_rows, r, epi_stage);
+            store_chunk16(g, un, q, lane, c0, epi_rows, r, epi_stage);
           }
           if (t == 0) a.cnt[un.tile] = 0;  // ready for the next call
         }
+      }
+      if (FUSED && g.signal_done) {
+        // the unit's rows are stored: count the tile done for its block (the barrier orders
+        // every epilogue thread's stores before thread 0's release increment)
+        named_bar_epi();
+        if (t == 0) red_release_add(g.signal_done + un.b, 1);
       }
       ++lu;
     }
@@ -549,11 +660,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + Cfg::kACol0;
     uint32_t it = 0;
     for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-      const Unit un = decode_unit(a, split_k, u);
+      const Unit un = decode_any<FUSED>(a, a2, split_k, units0_u, u);
       if (!un.ok) continue;
       // the tile's INT4 conversion (uniform over the unit, read while the weights are in flight)
+      const GemmArgs& ga = args_of<FUSED>(a, a2, un);
       const bool scaled =
-          __ldg(a.tile_mode + static_cast<int64_t>(un.e) * a.n_tiles + un.jt) == kTileScaled;
+          __ldg(ga.tile_mode + static_cast<int64_t>(un.e) * ga.n_tiles + un.jt) == kTileScaled;
+      const bool nvfp4 = ga.nvfp4 != 0;
       for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
         if (it % kDqGroups != static_cast<uint32_t>(g)) continue;
         const int nsub = min(KS, un.kb1 - kb);
@@ -580,7 +693,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&aempty[sa]), pa ^ 1, abort_flag, a.dev_err)))
           goto dq_done;
         tc_fence_after();
-        if (a.nvfp4) {
+        if (nvfp4) {
 #pragma unroll
           for (int sb = 0; sb < KS; ++sb) {
             if (sb < nsub) {
@@ -622,7 +735,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t nw = *w_issued, nb = *b_issued;
     for (uint32_t j = (nw > static_cast<uint32_t>(S_W) ? nw - S_W : 0); j < nw; ++j)
       mbar_wait_plain(smem_u32(&wfull[j % S_W]), (j / S_W) & 1);
-    if (!gather)
+    if (any_tma)
       for (uint32_t j = (nb > static_cast<uint32_t>(S_B) ? nb - S_B : 0); j < nb; ++j)
         mbar_wait_plain(smem_u32(&bfull[j % S_B]), (j / S_B) & 1);
   }
@@ -632,6 +745,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+}
+
+template <int NT, int KS>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ GemmArgs a) {
+  gemm_body<NT, KS, false>(a, a);
+}
+
+// Fused layer: the gate_up GEMM (a, SiLU-and-mul into sorted rows) and the down GEMM (a2, rows
+// of the first by TMA, top-k merge epilogue) walked as one persistent unit sequence.  Down
+// units wait per block for the gate_up tiles of that block, which earlier units of this grid
+// produce; the launch is cooperative so that every CTA is resident.
+template <int NT, int KS>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    moe_layer_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ GemmArgs a2) {
+  gemm_body<NT, KS, true>(a, a2);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -754,6 +883,53 @@ cudaError_t launch_gemm_t(GemmArgs& args, int grid, bool pdl, cudaStream_t strea
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, moe_gemm_kernel<NT, KS>, args);
+}
+
+template <int NT>
+cudaError_t launch_layer_t(GemmArgs& a, GemmArgs& a2, int grid, cudaStream_t stream) {
+  constexpr int KS = StageK<NT>::value;
+  using Cfg = GemmCfg<NT, KS>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t err = cudaFuncSetAttribute(moe_layer_kernel<NT, KS>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(Cfg::kSmemBytes));
+    if (err != cudaSuccess) return err;
+    configured = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;  // down units wait on other CTAs' gate_up units
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, moe_layer_kernel<NT, KS>, a, a2);
+}
+
+cudaError_t launch_layer_fused(GemmArgs& a, GemmArgs& a2, int grid, cudaStream_t stream) {
+  if (a.block_m != a2.block_m || a.split_k != 1 || a2.split_k != 1) return cudaErrorInvalidValue;
+  if (a.capacity <= 0) return cudaSuccess;
+  if (a.a_sorted) {
+    cudaError_t err = make_act_tmap(&a.tmap_a, a.A, a.capacity, a.K, a.lda, a.block_m);
+    if (err != cudaSuccess) return err;
+  }
+  if (a2.a_sorted) {
+    cudaError_t err = make_act_tmap(&a2.tmap_a, a2.A, a2.capacity, a2.K, a2.lda, a2.block_m);
+    if (err != cudaSuccess) return err;
+  }
+  switch (a.block_m) {
+    case 16: return launch_layer_t<16>(a, a2, grid, stream);
+    case 32: return launch_layer_t<32>(a, a2, grid, stream);
+    case 64: return launch_layer_t<64>(a, a2, grid, stream);
+    case 128: return launch_layer_t<128>(a, a2, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_gemm(GemmArgs& args, int grid, bool pdl, cudaStream_t stream) {

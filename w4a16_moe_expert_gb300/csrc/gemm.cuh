@@ -39,7 +39,15 @@ struct GemmArgs {
   int32_t* dev_err;
   int evict_first;
   int routing_ready;  // routing was complete before the previous kernel started
+  // fused layer only: the first GEMM counts finished tiles per block in signal_done; the
+  // second waits until wait_done[block] >= wait_count before loading that block's rows
+  int32_t* signal_done;
+  const int32_t* wait_done;
+  int wait_count;
 };
+
+// The fused layer call: gate_up (a) then down (a2) in one cooperative persistent launch.
+cudaError_t launch_layer_fused(GemmArgs& a, GemmArgs& a2, int grid, cudaStream_t stream);
 
 cudaError_t launch_gemm(GemmArgs& args, int grid, bool pdl, cudaStream_t stream);
 
