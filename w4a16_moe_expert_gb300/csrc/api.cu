@@ -336,6 +336,7 @@ static w4a16_status_t prepare_gemm(const GemmCall& c, const DeviceFacts& dev, Ge
   a.epilogue = c.epilogue;
   a.c_sorted = (c.row_flags & W4A16_C_ROWS_SORTED) ? 1 : 0;
   a.c_f32 = (c.row_flags & W4A16_C_FP32) ? 1 : 0;
+  a.c_st256 = (reinterpret_cast<uintptr_t>(c.C) % 32 == 0 && c.ldc % (a.c_f32 ? 8 : 16) == 0) ? 1 : 0;
   a.C = c.C;
   a.ldc = c.ldc;
   a.cnt = static_cast<int32_t*>(c.ws);

@@ -161,6 +161,18 @@ __device__ __forceinline__ float bf16_round(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
 }
 
+// 256-bit global stores (sm_100 and later; the address must be 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(float* p, float4 x, float4 y) {
+  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(x.x),
+               "f"(x.y), "f"(x.z), "f"(x.w), "f"(y.x), "f"(y.y), "f"(y.z), "f"(y.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_global_v8(uint16_t* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // Output row of token column j of the unit's block, or -1 when nothing is written there.
 __device__ __forceinline__ int64_t out_row(const GemmArgs& a, const Unit& un, int j, int32_t slot) {
   if (a.c_sorted) return static_cast<int64_t>(un.b) * a.block_m + j;  // padding rows get zeros
@@ -222,19 +234,37 @@ __device__ __forceinline__ void store_chunk16(const GemmArgs& a, const Unit& un,
           }
         }
       } else if (a.c_f32) {
-        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.C) + row * a.ldc + col);
+        float* dst = reinterpret_cast<float*>(a.C) + row * a.ldc + col;
+        if (a.c_st256) {  // 32-byte aligned rows: half the store instructions
 #pragma unroll
-        for (int k = 0; k < 4; ++k) dst[k] = routed ? src[k] : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int k = 0; k < 2; ++k) {
+            float4 x = src[2 * k], y = src[2 * k + 1];
+            if (!routed) x = y = make_float4(0.f, 0.f, 0.f, 0.f);
+            st_global_v8(dst + 8 * k, x, y);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            reinterpret_cast<float4*>(dst)[k] = routed ? src[k] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       } else {
-        uint4* dst = reinterpret_cast<uint4*>(a.C + row * a.ldc + col);
+        uint32_t w[8];
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const float4 x = src[2 * k], y = src[2 * k + 1];
+        for (int k = 0; k < 4; ++k) {
+          const float4 x = src[k];
           auto pk = [&](float lo, float hi2) {
             return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(routed ? lo : 0.f))) |
                    (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(routed ? hi2 : 0.f))) << 16);
           };
-          dst[k] = make_uint4(pk(x.x, x.y), pk(x.z, x.w), pk(y.x, y.y), pk(y.z, y.w));
+          w[2 * k] = pk(x.x, x.y);
+          w[2 * k + 1] = pk(x.z, x.w);
+        }
+        uint16_t* dst = a.C + row * a.ldc + col;
+        if (a.c_st256) {
+          st_global_v8(dst, w);
+        } else {
+          reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
         }
       }
     }

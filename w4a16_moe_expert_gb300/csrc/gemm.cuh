@@ -28,6 +28,7 @@ struct GemmArgs {
   int epilogue;
   int c_sorted;
   int c_f32;  // C is float (unrounded sums)
+  int c_st256;  // C and its rows are 32-byte aligned: the epilogue stores 32 bytes per lane
   const float* merge_w;  // non-null: add merge_w[slot] * value into C row slot / merge_k (FP32)
   int merge_k;
   uint16_t* C;
