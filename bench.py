@@ -50,7 +50,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 ROOFLINE_T = 64
 # Its DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum from an ncu capture
 # of that launch), valid only while the GEMM kernel's sources hash to the recorded value.
-ROOFLINE_TRAFFIC = {"sources_sha256": "5f62caa522ba0f43910c8a3b95e8f0c5a7499c41154d9593dc5b945522518467", "bytes": 223298816 + 3560448}
+ROOFLINE_TRAFFIC = {"sources_sha256": "db996ff25e0823ba2bb03a31e2e036b5baf765b8efe0ecf65396d4efecb55ead", "bytes": 223303168 + 3738880}
 GEMM_SOURCES = ("w4a16_moe_expert_gb300/csrc/gemm.cu", "w4a16_moe_expert_gb300/csrc/gemm.cuh",
                 "w4a16_moe_expert_gb300/csrc/common.cuh")
 
