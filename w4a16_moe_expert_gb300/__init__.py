@@ -68,7 +68,7 @@ class RoutingDesc(ctypes.Structure):
 
 
 class ScheduleDesc(ctypes.Structure):
-    _fields_ = [("split_k", ctypes.c_int32), ("num_ctas", ctypes.c_int32)]
+    _fields_ = [("split_k", ctypes.c_int32), ("num_ctas", ctypes.c_int32), ("cta_pairs", ctypes.c_int32)]
 
 
 class PlanDesc(ctypes.Structure):
@@ -306,7 +306,7 @@ def moe_gemm(A: torch.Tensor, a_row_div: int, W: PackedWeights, routing: Routing
              epilogue: int = EPILOGUE_NONE, row_flags: int = 0, out: Optional[torch.Tensor] = None,
              out_rows: Optional[int] = None, workspace: Optional[torch.Tensor] = None,
              expected_rows_per_expert: int = 0, split_k: int = 0, num_ctas: int = 0,
-             dev_err: Optional[torch.Tensor] = None) -> torch.Tensor:
+             dev_err: Optional[torch.Tensor] = None, cta_pairs: int = 0) -> torch.Tensor:
     _cuda(A, torch.bfloat16, "A")
     width = W.N // 2 if epilogue == EPILOGUE_SILU_MUL else W.N
     if out is None:
@@ -317,7 +317,7 @@ def moe_gemm(A: torch.Tensor, a_row_div: int, W: PackedWeights, routing: Routing
     _cuda(out, torch.float32 if row_flags & C_FP32 else torch.bfloat16, "out")
     if workspace is None:
         workspace = gemm_workspace(routing.total_slots, W.E, W.N, W.K, routing.block_m, A.device)
-    sched = ScheduleDesc(split_k, num_ctas)
+    sched = ScheduleDesc(split_k, num_ctas, cta_pairs)
     rd = routing.desc()
     _check("w4a16_moe_gemm", load().w4a16_moe_gemm(
         _ptr(A), A.stride(0), a_row_div, ctypes.byref(W.desc), ctypes.byref(rd), epilogue, row_flags,
@@ -355,7 +355,7 @@ def moe_gemm_static_scratch(A: torch.Tensor, a_row_div: int, W: PackedWeights, r
         out = torch.zeros((rows, width), dtype=torch.float32 if row_flags & C_FP32 else torch.bfloat16,
                           device=A.device)
     _cuda(out, torch.float32 if row_flags & C_FP32 else torch.bfloat16, "out")
-    sched = ScheduleDesc(split_k, num_ctas)
+    sched = ScheduleDesc(split_k, num_ctas, 0)
     rd = routing.desc()
     _check("w4a16_moe_gemm_static_scratch", load().w4a16_moe_gemm_static_scratch(
         _ptr(A), A.stride(0), a_row_div, ctypes.byref(W.desc), ctypes.byref(rd), epilogue, row_flags,

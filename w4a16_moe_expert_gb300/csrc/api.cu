@@ -257,6 +257,9 @@ struct GemmCall {
   int merge_k = 0;
 };
 
+// 128-token blocks use CTA pairs unless the schedule says otherwise.
+constexpr bool kPairsByDefault = false;
+
 // Checks a GEMM call and fills the kernel arguments and grid; *empty is set when there is
 // nothing to compute (no capacity or no experts).
 static w4a16_status_t prepare_gemm(const GemmCall& c, const DeviceFacts& dev, GemmArgs* out,
@@ -349,6 +352,18 @@ static w4a16_status_t prepare_gemm(const GemmCall& c, const DeviceFacts& dev, Ge
   a.routing_ready = c.routing_ready;
   a.merge_w = c.merge_w;
   a.merge_k = c.merge_k;
+  // CTA pairs (one M = 256 MMA over two CTAs' tiles) for 128-token blocks of sorted rows
+  const bool pair_ok = R->block_m == 128 && a.a_sorted && split == 1 && a.n_tiles % 2 == 0 &&
+                       grid >= 2 && !c.merge_w;
+  const int want_pair = c.sched ? c.sched->cta_pairs : 0;
+  if (want_pair == 2 && !pair_ok)
+    return fail(W4A16_INVALID_ARG, "CTA pairs need block_m 128, sorted activation rows, an even "
+                                   "tile count and no K split");
+  a.pair = (want_pair == 2 || (want_pair == 0 && pair_ok && kPairsByDefault)) ? 1 : 0;
+  if (a.pair) {
+    grid &= ~1;
+    fast_divisor(static_cast<uint32_t>(a.n_tiles / 2), &a.nt2_magic, &a.nt2_shift);
+  }
   *out_grid = grid;
   return W4A16_OK;
 }

@@ -48,9 +48,10 @@ constexpr int kGatherThreads = 64;  // warps 2 and 3 gather activation rows with
 // Three independent rings: packed weights in shared memory (freed once the dequant warps hold
 // them in registers), activation tiles in shared memory (freed by the MMA commit), dequantised
 // weights in TMEM (freed by the MMA commit).
-template <int NT, int KS>
+template <int NT, int KS, bool PAIR = false>
 struct GemmCfg {
-  static constexpr int kSubB = NT * 128;            // B bytes of one sub-block (NT rows x 64)
+  // B bytes of one sub-block (NT rows x 64; a CTA of a pair holds half the block's rows)
+  static constexpr int kSubB = (PAIR ? NT / 2 : NT) * 128;
   static constexpr int kBBytes = KS * kSubB;        // one activation stage
   static constexpr int kWBytes = KS * kChunkBytes;  // one weight stage
   // activation ring: 64-96 KB (at least 4, at most 24 stages), the rest for weights.  The
@@ -113,11 +114,30 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int split_k, int6
   return t;
 }
 
+// CTA pairs: unit u = (block, pair of 128-row tiles); CTA rank r of the pair takes tile
+// 2 * pair + r.  No K splits.
+__device__ __forceinline__ Unit decode_unit_pair(const GemmArgs& a, uint32_t crank, int64_t u64) {
+  const uint32_t u = static_cast<uint32_t>(u64);
+  Unit t;
+  const uint32_t b = (__umulhi(u, a.nt2_magic) + u) >> a.nt2_shift;
+  t.tile = u;
+  t.b = static_cast<int>(b);
+  t.jt = static_cast<int>(2 * (u - b * static_cast<uint32_t>(a.n_tiles >> 1)) + crank);
+  t.split = 0;
+  t.kb0 = 0;
+  t.kb1 = a.n_kb;
+  t.gi = 0;
+  t.e = __ldg(a.expert_ids + t.b);
+  t.ok = t.e >= 0 && t.e < a.E;
+  return t;
+}
+
 // Fused layer: units [0, units0) are the first GEMM's (gate_up), the rest the second's (down),
 // both over the same aligned blocks.  A plain call has one GEMM (a2 is a).
-template <bool FUSED>
+template <bool FUSED, bool PAIR = false>
 __device__ __forceinline__ Unit decode_any(const GemmArgs& a, const GemmArgs& a2, int split_k,
-                                           uint32_t units0, int64_t u64) {
+                                           uint32_t units0, uint32_t crank, int64_t u64) {
+  if (PAIR) return decode_unit_pair(a, crank, u64);
   if (!FUSED) return decode_unit(a, split_k, u64);
   const uint32_t u = static_cast<uint32_t>(u64);
   if (u < units0) return decode_unit(a, 1, u);
@@ -272,9 +292,43 @@ __device__ __forceinline__ void store_chunk16(const GemmArgs& a, const Unit& un,
   __syncwarp();  // the staging area is reused by the next chunk
 }
 
-template <int NT, int KS, bool FUSED>
+// Waits in a pair kernel acquire at cluster scope (peers arrive on the even CTA's barriers).
+template <bool PAIR>
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         int32_t* dev_err) {
+  return PAIR ? mbar_wait_cl(bar, parity, abort_flag, dev_err) : mbar_wait(bar, parity, abort_flag, dev_err);
+}
+template <bool PAIR>
+__device__ __forceinline__ bool wait_bar_plain(uint32_t bar, uint32_t parity) {
+  return PAIR ? mbar_wait_plain_cl(bar, parity) : mbar_wait_plain(bar, parity);
+}
+
+template <bool PAIR>
+__device__ __forceinline__ void mma_any(uint32_t d, uint32_t a_tmem, uint64_t bd, uint32_t idesc,
+                                        uint32_t acc) {
+  if (PAIR) mma_ts_pair(d, a_tmem, bd, idesc, acc); else mma_ts(d, a_tmem, bd, idesc, acc);
+}
+template <bool PAIR>
+__device__ __forceinline__ void commit_any(uint32_t bar) {
+  if (PAIR) mma_commit_pair(bar); else mma_commit(bar);
+}
+// A hand-off arrival from a warp: in a pair kernel lane 0 arrives for the warp on the even
+// CTA's barrier (locally or remotely); otherwise every thread arrives locally.
+template <bool PAIR>
+__device__ __forceinline__ void arrive_handoff(uint32_t bar, bool leader, int lane) {
+  if (PAIR) {
+    __syncwarp();
+    if (lane == 0) {
+      if (leader) mbar_arrive(bar); else mbar_arrive_remote(mapa_shared(bar, 0));
+    }
+  } else {
+    mbar_arrive(bar);
+  }
+}
+
+template <int NT, int KS, bool FUSED, bool PAIR = false>
 __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2) {
-  using Cfg = GemmCfg<NT, KS>;
+  using Cfg = GemmCfg<NT, KS, PAIR>;
   constexpr int S_W = Cfg::kWStages;
   constexpr int S_B = Cfg::kBStages;
   constexpr int S_A = Cfg::kAStages;
@@ -305,6 +359,12 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       (reinterpret_cast<uintptr_t>(epi_rows + NT) + 15) & ~static_cast<uintptr_t>(15));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // CTA pairs: the even CTA of each two-CTA cluster issues the MMAs; the odd one forwards its
+  // activation tiles' arrival and its dequant / epilogue hand-offs to the even CTA's barriers
+  const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = crank == 0;
+  const int64_t unit0 = PAIR ? (blockIdx.x >> 1) : blockIdx.x;
+  const int64_t ustride = PAIR ? (gridDim.x >> 1) : gridDim.x;
   const bool gather = !a.a_sorted;
   // a fused call may mix gathered and TMA-loaded activations (one GEMM each): every stage then
   // completes on 64 arrivals, the TMA path's lane 0 also expecting the tile's bytes
@@ -316,16 +376,16 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       mbar_init(smem_u32(&wempty[s]), 4);
     }
     for (int s = 0; s < S_B; ++s) {
-      mbar_init(smem_u32(&bfull[s]), (FUSED || gather) ? kGatherThreads : 1);
+      mbar_init(smem_u32(&bfull[s]), PAIR ? (leader ? 2 : 1) : ((FUSED || gather) ? kGatherThreads : 1));
       mbar_init(smem_u32(&bempty[s]), 1);
     }
     for (int s = 0; s < S_A; ++s) {
-      mbar_init(smem_u32(&afull[s]), 128);
+      mbar_init(smem_u32(&afull[s]), PAIR ? 8 : 128);  // pairs: one arrival per warp of both CTAs
       mbar_init(smem_u32(&aempty[s]), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&accfull[s]), 1);
-      mbar_init(smem_u32(&accempty[s]), 128);
+      mbar_init(smem_u32(&accempty[s]), PAIR ? 8 : 128);
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
@@ -339,11 +399,17 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
     if (FUSED && a2.a_sorted) tma_prefetch_desc(&a2.tmap_a);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // both CTAs' barriers exist before either arrives on the other's
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -359,7 +425,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
   // Fewer K splits when the routed blocks would overflow the partial-sum scratch.
   int split_k = a.split_k;
   while (split_k > 1 && nblocks * a.n_tiles * split_k > a.max_split_units) --split_k;
-  const int64_t units0 = nblocks * a.n_tiles * split_k;
+  const int64_t units0 = PAIR ? nblocks * (a.n_tiles >> 1) : nblocks * a.n_tiles * split_k;
   const int64_t n_units = FUSED ? units0 + nblocks * a2.n_tiles : units0;
   const uint32_t units0_u = static_cast<uint32_t>(units0);
 
@@ -370,8 +436,8 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
     // Weights never depend on the previous kernel, so they stream before pdl_wait.
     const uint64_t policy = a.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
     uint32_t it = 0;
-    for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-      const Unit un = decode_any<FUSED>(a, a2, split_k, units0_u, u);
+    for (int64_t u = PAIR ? unit0 : blockIdx.x; u < n_units; u += PAIR ? ustride : gridDim.x) {
+      const Unit un = decode_any<FUSED, PAIR>(a, a2, split_k, units0_u, crank, u);
       if (!un.ok) continue;
       const GemmArgs& g = args_of<FUSED>(a, a2, un);
       const uint8_t* strip = g.wblob + kHeaderBytes +
@@ -380,7 +446,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
         const int nsub = min(KS, un.kb1 - kb);
         const int s = it % S_W;
         const uint32_t ph = (it / S_W) & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&wempty[s]), ph ^ 1, abort_flag, a.dev_err)))
+        if (!__all_sync(0xffffffffu, wait_bar<PAIR>(smem_u32(&wempty[s]), ph ^ 1, abort_flag, a.dev_err)))
           goto wprod_done;
         if (lane == static_cast<int>(it & 31)) {
           const uint32_t wb = smem_u32(&wfull[s]);
@@ -405,8 +471,8 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       const int gt = tid - 64;
       const int c = gt & 7;
       constexpr int R = NT / 8;
-      for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const Unit un = decode_any<FUSED>(a, a2, split_k, units0_u, u);
+      for (int64_t u = PAIR ? unit0 : blockIdx.x; u < n_units; u += PAIR ? ustride : gridDim.x) {
+        const Unit un = decode_any<FUSED, PAIR>(a, a2, split_k, units0_u, crank, u);
         if (!un.ok) continue;
         const GemmArgs& g = args_of<FUSED>(a, a2, un);
         if (g.wait_done) {
@@ -426,7 +492,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
             const int nsub = min(KS, un.kb1 - kb);
             const int s = it % S_B;
             const uint32_t ph = (it / S_B) & 1;
-            if (!mbar_wait(smem_u32(&bempty[s]), ph ^ 1, abort_flag, g.dev_err)) goto fprod_done;
+            if (!wait_bar<PAIR>(smem_u32(&bempty[s]), ph ^ 1, abort_flag, g.dev_err)) goto fprod_done;
             const uint32_t bdst = smem_u32(b_ring + s * Cfg::kBBytes);
             for (int sb = 0; sb < nsub; ++sb) {
 #pragma unroll
@@ -444,7 +510,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
             const int nsub = min(KS, un.kb1 - kb);
             const int s = it % S_B;
             const uint32_t ph = (it / S_B) & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bempty[s]), ph ^ 1, abort_flag, g.dev_err)))
+            if (!__all_sync(0xffffffffu, wait_bar<PAIR>(smem_u32(&bempty[s]), ph ^ 1, abort_flag, g.dev_err)))
               goto fprod_done;
             const uint32_t bb = smem_u32(&bfull[s]);
             if (gt == 0)
@@ -470,8 +536,8 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       const int g = tid - 64;
       const int c = g & 7;  // 16-byte chunk of a 128-byte row handled by this thread
       constexpr int R = NT / 8;  // rows per thread: (g >> 3) + 8j
-      for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const Unit un = decode_any<FUSED>(a, a2, split_k, units0_u, u);
+      for (int64_t u = PAIR ? unit0 : blockIdx.x; u < n_units; u += PAIR ? ustride : gridDim.x) {
+        const Unit un = decode_any<FUSED, PAIR>(a, a2, split_k, units0_u, crank, u);
         if (!un.ok) continue;
         int32_t arow[R];
 #pragma unroll
@@ -483,7 +549,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
           const int nsub = min(KS, un.kb1 - kb);
           const int s = it % S_B;
           const uint32_t ph = (it / S_B) & 1;
-          if (!mbar_wait(smem_u32(&bempty[s]), ph ^ 1, abort_flag, a.dev_err)) goto bprod_done;
+          if (!wait_bar<PAIR>(smem_u32(&bempty[s]), ph ^ 1, abort_flag, a.dev_err)) goto bprod_done;
           const uint32_t bdst = smem_u32(b_ring + s * Cfg::kBBytes);
           // Padding rows are not loaded: MMA column j reads only B row j, so whatever a
           // padding row holds lands in a token column that the epilogue discards.
@@ -503,14 +569,14 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       cp_async_wait_all();
     } else if (warp == 2) {
       // rows already in sorted order: one 2-D TMA tile per K sub-block, rotating lanes
-      for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const Unit un = decode_any<FUSED>(a, a2, split_k, units0_u, u);
+      for (int64_t u = PAIR ? unit0 : blockIdx.x; u < n_units; u += PAIR ? ustride : gridDim.x) {
+        const Unit un = decode_any<FUSED, PAIR>(a, a2, split_k, units0_u, crank, u);
         if (!un.ok) continue;
         for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
           const int nsub = min(KS, un.kb1 - kb);
           const int s = it % S_B;
           const uint32_t ph = (it / S_B) & 1;
-          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bempty[s]), ph ^ 1, abort_flag, a.dev_err)))
+          if (!__all_sync(0xffffffffu, wait_bar<PAIR>(smem_u32(&bempty[s]), ph ^ 1, abort_flag, a.dev_err)))
             goto tprod_done;
           const uint32_t bb = smem_u32(&bfull[s]);
           if (lane == 0) mbar_arrive_expect_tx(bb, nsub * Cfg::kSubB);
@@ -518,7 +584,8 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
           for (int sb = 0; sb < nsub; ++sb)
             if (lane == static_cast<int>((it * KS + sb) & 31))
               tma_load_2d(smem_u32(b_ring + s * Cfg::kBBytes + sb * Cfg::kSubB), &a.tmap_a,
-                          (kb + sb) * kBlockK, static_cast<int>(un.b * a.block_m), bb);
+                          (kb + sb) * kBlockK,
+                          static_cast<int>(un.b * a.block_m + (PAIR ? crank * (NT / 2) : 0)), bb);
           __syncwarp();
         }
       }
@@ -530,17 +597,35 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
     // Measured on GB300: a burst of MMAs issued from a fully unrolled sequence inside one
     // long-lived elected region costs ~9 cycles per N=16 MMA, while re-electing every stage or
     // issuing from a rolled loop costs several hundred cycles per stage.
-    constexpr uint32_t idesc = idesc_bf16_f32(128, NT);
+    constexpr uint32_t idesc = idesc_bf16_f32(PAIR ? 256 : 128, NT);
     const uint64_t b_desc0 = smem_desc_sw128(smem_u32(b_ring));
-    if (elect_one()) {
+    if (PAIR && !leader) {
+      // odd CTA of a pair: pass each landed activation stage on to the even CTA's barrier,
+      // then wait for the pair's last MMAs before the TMEM they write is released
+      if (elect_one()) {
+        uint32_t it = 0;
+        for (int64_t u = PAIR ? unit0 : blockIdx.x; u < n_units; u += PAIR ? ustride : gridDim.x) {
+          const Unit un = decode_any<FUSED, PAIR>(a, a2, split_k, units0_u, crank, u);
+          if (!un.ok) continue;
+          for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
+            const int sbi = it % S_B;
+            const uint32_t pb = (it / S_B) & 1;
+            if (!wait_bar<PAIR>(smem_u32(&bfull[sbi]), pb, abort_flag, a.dev_err)) goto fwd_done;
+            mbar_arrive_remote(mapa_shared(smem_u32(&bfull[sbi]), 0));
+          }
+        }
+      fwd_done:
+        wait_bar_plain<PAIR>(smem_u32(drain), 0);
+      }
+    } else if (elect_one()) {
       uint32_t it = 0, lu = 0;
-      for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const Unit un = decode_any<FUSED>(a, a2, split_k, units0_u, u);
+      for (int64_t u = PAIR ? unit0 : blockIdx.x; u < n_units; u += PAIR ? ustride : gridDim.x) {
+        const Unit un = decode_any<FUSED, PAIR>(a, a2, split_k, units0_u, crank, u);
         if (!un.ok) continue;
         const bool rows_gathered = FUSED ? !args_of<FUSED>(a, a2, un).a_sorted : gather;
         const int ab = lu & 1;
         const uint32_t pab = (lu >> 1) & 1;
-        if (!mbar_wait(smem_u32(&accempty[ab]), pab ^ 1, abort_flag, a.dev_err)) goto mma_done;
+        if (!wait_bar<PAIR>(smem_u32(&accempty[ab]), pab ^ 1, abort_flag, a.dev_err)) goto mma_done;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + ab * NT;
         for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
@@ -549,8 +634,8 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
           const uint32_t pb = (it / S_B) & 1;
           const int sa = it % S_A;
           const uint32_t pa = (it / S_A) & 1;
-          if (!mbar_wait(smem_u32(&afull[sa]), pa, abort_flag, a.dev_err)) goto mma_done;
-          if (!mbar_wait(smem_u32(&bfull[sbi]), pb, abort_flag, a.dev_err)) goto mma_done;
+          if (!wait_bar<PAIR>(smem_u32(&afull[sa]), pa, abort_flag, a.dev_err)) goto mma_done;
+          if (!wait_bar<PAIR>(smem_u32(&bfull[sbi]), pb, abort_flag, a.dev_err)) goto mma_done;
           if (rows_gathered) fence_proxy_async_smem();  // cp.async (generic proxy) rows -> tensor core
           tc_fence_after();
           const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((sbi * Cfg::kBBytes) >> 4);
@@ -561,30 +646,30 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
             for (int sb = 0; sb < KS; ++sb) {
               const uint64_t bd = b_desc + static_cast<uint64_t>((sb * Cfg::kSubB) >> 4);
               const uint32_t at = a_tmem + sb * 32;
-              mma_ts(d_tmem, at, bd, idesc, sb > 0 ? 1u : acc0);
-              mma_ts(d_tmem, at + 8, bd + 2, idesc, 1u);
-              mma_ts(d_tmem, at + 16, bd + 4, idesc, 1u);
-              mma_ts(d_tmem, at + 24, bd + 6, idesc, 1u);
+              mma_any<PAIR>(d_tmem, at, bd, idesc, sb > 0 ? 1u : acc0);
+              mma_any<PAIR>(d_tmem, at + 8, bd + 2, idesc, 1u);
+              mma_any<PAIR>(d_tmem, at + 16, bd + 4, idesc, 1u);
+              mma_any<PAIR>(d_tmem, at + 24, bd + 6, idesc, 1u);
             }
           } else {  // K tail shorter than a full stage
             for (int sb = 0; sb < nsub; ++sb) {
               const uint64_t bd = b_desc + static_cast<uint64_t>((sb * Cfg::kSubB) >> 4);
               const uint32_t at = a_tmem + sb * 32;
-              mma_ts(d_tmem, at, bd, idesc, sb > 0 ? 1u : acc0);
-              mma_ts(d_tmem, at + 8, bd + 2, idesc, 1u);
-              mma_ts(d_tmem, at + 16, bd + 4, idesc, 1u);
-              mma_ts(d_tmem, at + 24, bd + 6, idesc, 1u);
+              mma_any<PAIR>(d_tmem, at, bd, idesc, sb > 0 ? 1u : acc0);
+              mma_any<PAIR>(d_tmem, at + 8, bd + 2, idesc, 1u);
+              mma_any<PAIR>(d_tmem, at + 16, bd + 4, idesc, 1u);
+              mma_any<PAIR>(d_tmem, at + 24, bd + 6, idesc, 1u);
             }
           }
-          mma_commit(smem_u32(&bempty[sbi]));
-          mma_commit(smem_u32(&aempty[sa]));
+          commit_any<PAIR>(smem_u32(&bempty[sbi]));
+          commit_any<PAIR>(smem_u32(&aempty[sa]));
         }
-        mma_commit(smem_u32(&accfull[ab]));
+        commit_any<PAIR>(smem_u32(&accfull[ab]));
         ++lu;
       }
     mma_done:
-      mma_commit(smem_u32(drain));
-      mbar_wait_plain(smem_u32(drain), 0);
+      commit_any<PAIR>(smem_u32(drain));
+      wait_bar_plain<PAIR>(smem_u32(drain), 0);
     }
     __syncwarp();
   } else if (warp >= 4 && warp < 8) {
@@ -594,8 +679,8 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
     const int t = q * 32 + lane;  // tile row = TMEM lane
     uint8_t* epi_stage = epi_stage_base + q * kEpiStageBytes;
     uint32_t lu = 0;
-    for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-      const Unit un = decode_any<FUSED>(a, a2, split_k, units0_u, u);
+    for (int64_t u = PAIR ? unit0 : blockIdx.x; u < n_units; u += PAIR ? ustride : gridDim.x) {
+      const Unit un = decode_any<FUSED, PAIR>(a, a2, split_k, units0_u, crank, u);
       if (!un.ok) continue;
       const GemmArgs& g = args_of<FUSED>(a, a2, un);
       named_bar_epi();  // the previous unit's readers of epi_rows / last_flag are done
@@ -603,7 +688,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       named_bar_epi();
       const int ab = lu & 1;
       const uint32_t pab = (lu >> 1) & 1;
-      const bool ok = mbar_wait(smem_u32(&accfull[ab]), pab, abort_flag, a.dev_err);
+      const bool ok = wait_bar<PAIR>(smem_u32(&accfull[ab]), pab, abort_flag, a.dev_err);
       if (epi_any(!ok)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ab * NT;
@@ -618,7 +703,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
           if (c0 + 16 < NT) tmem_ld16(taddr + c0 + 16, r1);
           if (c0 + 16 >= NT) {
             tc_fence_before();
-            mbar_arrive(smem_u32(&accempty[ab]));
+            arrive_handoff<PAIR>(smem_u32(&accempty[ab]), leader, lane);
           }
           store_chunk16(g, un, q, lane, c0, epi_rows, r0, epi_stage);
           if (c0 + 16 < NT) {
@@ -626,7 +711,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
             if (c0 + 32 < NT) tmem_ld16(taddr + c0 + 32, r0);
             if (c0 + 32 >= NT) {
               tc_fence_before();
-              mbar_arrive(smem_u32(&accempty[ab]));
+              arrive_handoff<PAIR>(smem_u32(&accempty[ab]), leader, lane);
             }
             store_chunk16(g, un, q, lane, c0 + 16, epi_rows, r1, epi_stage);
           }
@@ -640,7 +725,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
           tmem_wait_ld16(r);
           if (c0 + 16 >= NT) {
             tc_fence_before();
-            mbar_arrive(smem_u32(&accempty[ab]));
+            arrive_handoff<PAIR>(smem_u32(&accempty[ab]), leader, lane);
           }
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) __stcg(part + (c0 + jj) * 128 + t, __uint_as_float(r[jj]));
@@ -689,8 +774,8 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
     const int t = q * 32 + lane;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + Cfg::kACol0;
     uint32_t it = 0;
-    for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-      const Unit un = decode_any<FUSED>(a, a2, split_k, units0_u, u);
+    for (int64_t u = PAIR ? unit0 : blockIdx.x; u < n_units; u += PAIR ? ustride : gridDim.x) {
+      const Unit un = decode_any<FUSED, PAIR>(a, a2, split_k, units0_u, crank, u);
       if (!un.ok) continue;
       // the tile's INT4 conversion (uniform over the unit, read while the weights are in flight)
       const GemmArgs& ga = args_of<FUSED>(a, a2, un);
@@ -705,7 +790,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
         const int sa = it % S_A;
         const uint32_t pa = (it / S_A) & 1;
         // warp-uniform decisions: tcgen05.st below is a warp-collective instruction
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&wfull[sw]), pw, abort_flag, a.dev_err)))
+        if (!__all_sync(0xffffffffu, wait_bar<PAIR>(smem_u32(&wfull[sw]), pw, abort_flag, a.dev_err)))
           goto dq_done;
         uint4 lo[KS], hi[KS];
         uint32_t s2[KS];
@@ -720,7 +805,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
         }
         __syncwarp();  // every lane holds its rows: the weight stage may be refilled
         if (lane == 0) mbar_arrive(smem_u32(&wempty[sw]));
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&aempty[sa]), pa ^ 1, abort_flag, a.dev_err)))
+        if (!__all_sync(0xffffffffu, wait_bar<PAIR>(smem_u32(&aempty[sa]), pa ^ 1, abort_flag, a.dev_err)))
           goto dq_done;
         tc_fence_after();
         if (nvfp4) {
@@ -753,7 +838,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(smem_u32(&afull[sa]));
+        arrive_handoff<PAIR>(smem_u32(&afull[sa]), leader, lane);
       }
     }
   dq_done:;
@@ -764,16 +849,17 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
     // give in-flight copies a bounded chance to land before the CTA's memory goes away
     const uint32_t nw = *w_issued, nb = *b_issued;
     for (uint32_t j = (nw > static_cast<uint32_t>(S_W) ? nw - S_W : 0); j < nw; ++j)
-      mbar_wait_plain(smem_u32(&wfull[j % S_W]), (j / S_W) & 1);
+      wait_bar_plain<PAIR>(smem_u32(&wfull[j % S_W]), (j / S_W) & 1);
     if (any_tma)
       for (uint32_t j = (nb > static_cast<uint32_t>(S_B) ? nb - S_B : 0); j < nb; ++j)
-        mbar_wait_plain(smem_u32(&bfull[j % S_B]), (j / S_B) & 1);
+        wait_bar_plain<PAIR>(smem_u32(&bfull[j % S_B]), (j / S_B) & 1);
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // the peer is done with the pair's TMEM and barriers
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if (PAIR) tmem_dealloc_pair(tmem_base, kTmemCols); else tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -781,6 +867,14 @@ template <int NT, int KS>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmArgs a) {
   gemm_body<NT, KS, false>(a, a);
+}
+
+// CTA pairs (128-token blocks): launched as two-CTA clusters; one M = 256 MMA covers the two
+// CTAs' 128-row weight tiles, each CTA holding half of the block's activation rows.
+template <int NT, int KS>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    moe_gemm_pair_kernel(const __grid_constant__ GemmArgs a) {
+  gemm_body<NT, KS, false, true>(a, a);
 }
 
 // Fused layer: the gate_up GEMM (a, SiLU-and-mul into sorted rows) and the down GEMM (a2, rows
@@ -962,7 +1056,43 @@ cudaError_t launch_layer_fused(GemmArgs& a, GemmArgs& a2, int grid, cudaStream_t
   }
 }
 
+static cudaError_t launch_gemm_pair(GemmArgs& args, int grid, bool pdl, cudaStream_t stream) {
+  constexpr int NT = 128, KS = StageK<NT>::value;
+  using Cfg = GemmCfg<NT, KS, true>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t err = cudaFuncSetAttribute(moe_gemm_pair_kernel<NT, KS>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(Cfg::kSmemBytes));
+    if (err != cudaSuccess) return err;
+    configured = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid & ~1);
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, moe_gemm_pair_kernel<NT, KS>, args);
+}
+
 cudaError_t launch_gemm(GemmArgs& args, int grid, bool pdl, cudaStream_t stream) {
+  if (args.pair) {  // block_m 128, sorted rows, even tile count, no K split (checked by the caller)
+    if (args.block_m != 128 || !args.a_sorted || args.split_k != 1 || args.n_tiles % 2 || grid < 2)
+      return cudaErrorInvalidValue;
+    cudaError_t err = make_act_tmap(&args.tmap_a, args.A, args.capacity, args.K, args.lda,
+                                    args.block_m / 2);
+    if (err != cudaSuccess) return err;
+    return launch_gemm_pair(args, grid, pdl, stream);
+  }
   const int64_t rows = args.a_sorted
                            ? args.capacity
                            : (static_cast<int64_t>(args.total_slots) + args.a_row_div - 1) /

@@ -45,12 +45,15 @@ struct GemmArgs {
   int32_t* signal_done;
   const int32_t* wait_done;
   int wait_count;
+  // CTA pairs (block_m 128): units are (block, pair of 128-row tiles); divisor n_tiles / 2
+  int pair;
+  uint32_t nt2_magic, nt2_shift;
 };
 
 // The fused layer call: gate_up (a) then down (a2) in one cooperative persistent launch.
 cudaError_t launch_layer_fused(GemmArgs& a, GemmArgs& a2, int grid, cudaStream_t stream);
 
-cudaError_t launch_gemm(GemmArgs& args, int grid, bool pdl, cudaStream_t stream);
+cudaError_t launch_gemm(GemmArgs& args, int grid, bool pdl, cudaStream_t stream);  // pairs if args.pair
 
 // Multiply-shift constants for dividing 31-bit numerators by d >= 1 (round-up reciprocal).
 inline void fast_divisor(uint32_t d, uint32_t* magic, uint32_t* shift) {
