@@ -50,7 +50,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 ROOFLINE_T = 64
 # Its DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum from an ncu capture
 # of that launch), valid only while the GEMM kernel's sources hash to the recorded value.
-ROOFLINE_TRAFFIC = {"sources_sha256": "db996ff25e0823ba2bb03a31e2e036b5baf765b8efe0ecf65396d4efecb55ead", "bytes": 223303168 + 3738880}
+ROOFLINE_TRAFFIC = {"sources_sha256": "34747edaeb069fa4cc3acfd762d0c1ddad1b8a3a09648f3892574f5a093d84ac", "bytes": 223309824 + 3368192}
 GEMM_SOURCES = ("w4a16_moe_expert_gb300/csrc/gemm.cu", "w4a16_moe_expert_gb300/csrc/gemm.cuh",
                 "w4a16_moe_expert_gb300/csrc/common.cuh")
 
@@ -469,6 +469,24 @@ def run_ours(args, rank, world, local_rank):
                 "T": small["T"], "G": wl.E, "max_m": max_m, "expected_m": exp_m, "us": round(t_m, 2),
                 "weight_GBps": round(small["acct"]["gate_up"]["weight_bytes"] / t_m / 1e3, 1)}
         extras["grouped_contracts"] = grouped
+
+        # CTA pairs (tcgen05 cta_group::2, M = 256) on the 128-token-block calls, same method
+        pair_rows = []
+        for c in cases:
+            if c["block_m"] != 128 or (2 * wl.I // 128) % 2 or (wl.H // 128) % 2:
+                continue
+            r, hint = c["routing"], rows_hint[c["T"]]
+            gu = per_call_us(lambda i: (lib.gather_rows(c["x"], wl.top_k, r, out=c["xs"]), lib.moe_gemm(
+                c["xs"], 1, w13s[i % c["n_gu"]], r, epilogue=lib.EPILOGUE_SILU_MUL,
+                row_flags=lib.A_ROWS_SORTED | lib.C_ROWS_SORTED, out=c["h"], workspace=c["ws"],
+                expected_rows_per_expert=hint, cta_pairs=2)), c["R_gu"])
+            dn = per_call_us(lambda i: lib.moe_gemm(
+                c["h"], 1, w2s[i % c["n_dn"]], r, row_flags=lib.A_ROWS_SORTED | lib.C_FP32,
+                out=c["y"], workspace=c["ws"], expected_rows_per_expert=hint, cta_pairs=2), c["R_dn"])
+            pair_rows.append({"T": c["T"], "gate_up_us": round(gu, 2), "down_us": round(dn, 2)})
+        extras["cta_pairs"] = {
+            "what": "128-token-block calls with CTA pairs (one M=256 tcgen05 MMA over two CTAs' tiles)",
+            "sweep": pair_rows}
 
     # e2e through the public layer call, host buffers, copies inside the timed region
     e2e_events = []
