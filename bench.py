@@ -79,6 +79,19 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(values, world, device):
+    """Element-wise maximum of per-rank timings: the slowest replica bounds the whole job."""
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def whole_job_gbps(bytes_per_rank, world, us):
+    """GB/s of the whole job: every replica moves bytes_per_rank in (at most) `us` microseconds."""
+    return bytes_per_rank * world / (us * 1e-6) / 1e9
+
+
 # ---- per-T algorithmic accounting -----------------------------------------------------------
 
 def accounting(wl, T, topk_ids):
@@ -520,13 +533,11 @@ def run_ours(args, rank, world, local_rank):
     tflops_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
 
     # max over ranks of the timed device time; value sums the ranks' work
-    t_dev = torch.tensor([gemm_us, step_ms, wall], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t_dev, op=torch.distributed.ReduceOp.MAX)
-    gemm_us_max, step_ms_max = float(t_dev[0]), float(t_dev[1])
-    value = w_bytes * world / (gemm_us_max * 1e-6) / 1e9
+    gemm_us_max, step_ms_max, _, e2e_us_max = max_over_ranks([gemm_us, step_ms, wall, sum(e2e_us)],
+                                                             world, dev)
+    value = whole_job_gbps(w_bytes, world, gemm_us_max)
     achieved = alg_bytes / (gemm_us_max * 1e-6) / 1e9
-    e2e_value = w_bytes * world / (sum(e2e_us) * 1e-6) / 1e9
+    e2e_value = whole_job_gbps(w_bytes, world, e2e_us_max)
 
     # roofline of one launch: the gate_up GEMM at ROOFLINE_T tokens (else the smallest T above
     # one), algorithmic bytes over its per-call time
