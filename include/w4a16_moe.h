@@ -314,8 +314,10 @@ w4a16_status_t w4a16_topk_sum(const float* Y, const int32_t* topk_ids,
  * loads wait until all gate_up tiles of its block are stored (a per-block counter in the
  * workspace, bounded wait), while its weights stream from the start, so the down projection
  * overlaps the gate_up tail.  The launch is cooperative (all CTAs resident); a wait that runs
- * out sets W4A16_DEVERR_TIMEOUT.  Kernels: align, (row gather for block_m >= 64), zeroing, the
- * fused GEMM, rounding.  Not bitwise reproducible, as for W4A16_LAYER_FUSED_TOPK; implies it. */
+ * out sets W4A16_DEVERR_TIMEOUT.  The kernel also zeroes the FP32 token sums first and rounds
+ * them into out last (grid-wide phase counts; the align kernel clears the counts each call).
+ * Kernels: align, (row gather for block_m >= 64), the fused GEMM.  Not bitwise reproducible,
+ * as for W4A16_LAYER_FUSED_TOPK; implies it. */
 #define W4A16_LAYER_FUSED 0x2u
 int w4a16_plan_block_m(int T, int top_k, int E, int E_global);
 size_t w4a16_layer_workspace_size(int T, int top_k, int E, int E_global, int H, int I,

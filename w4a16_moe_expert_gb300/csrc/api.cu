@@ -202,25 +202,6 @@ static void pdl_config(int64_t work_items, int num_sms, cudaStream_t stream, cud
   cfg->numAttrs = 1;
 }
 
-// Zeroes n floats at p and m 32-bit words at q (both 16-byte aligned, n and m multiples of 4).
-__global__ void __launch_bounds__(256)
-    zero2_kernel(float* __restrict__ p, int64_t n4, int32_t* __restrict__ q, int64_t m4) {
-  pdl_wait();  // the previous call's last kernel may still read these buffers
-  pdl_launch_dependents();
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (int64_t i = i0; i < n4; i += stride) reinterpret_cast<float4*>(p)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int64_t i = i0; i < m4; i += stride) reinterpret_cast<int4*>(q)[i] = make_int4(0, 0, 0, 0);
-}
-
-static cudaError_t launch_zero2(float* p, int64_t n, int32_t* q, int64_t m, int num_sms,
-                                cudaStream_t stream) {
-  cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[1];
-  pdl_config(std::max(n, m) / 4, num_sms, stream, &cfg, attr);
-  return cudaLaunchKernelEx(&cfg, zero2_kernel, p, n / 4, q, m / 4);
-}
-
 static cudaError_t launch_zero_f32(float* p, int64_t n, int num_sms, cudaStream_t stream) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
@@ -709,6 +690,12 @@ struct LayerLayout {
   size_t off_sorted, off_expert, off_ntp, off_cnt, off_part, off_xs, off_h, off_y, off_done, total;
 };
 
+// Words of the single-kernel layer's counters (per-block gate_up tiles, zeroed sums, finished
+// CTAs), a multiple of 4.
+static size_t done_words(const LayerLayout& L) {
+  return round_up(static_cast<size_t>(L.cap / L.block_m) + 2, 4);
+}
+
 static LayerLayout layer_layout(int T, int top_k, int E, int E_global, int H, int I, int block_m) {
   LayerLayout L{};
   L.block_m = block_m > 0 ? block_m : w4a16_plan_block_m(T, top_k, E, E_global);
@@ -730,8 +717,8 @@ static LayerLayout layer_layout(int T, int top_k, int E, int E_global, int H, in
   o = round_up(o + static_cast<size_t>(L.cap) * I * 2, 256);
   L.off_y = o;
   o = round_up(o + static_cast<size_t>(T) * top_k * H * 4, 256);
-  L.off_done = o;  // fused layer: finished gate_up tiles per block (multiple of 4 words)
-  o = round_up(o + round_up(static_cast<size_t>(L.cap / L.block_m), 4) * 4, 256);
+  L.off_done = o;  // single-kernel layer: finished gate_up tiles per block, then 2 phase counts
+  o = round_up(o + done_words(L) * 4, 256);
   L.total = o;
   return L;
 }
@@ -794,18 +781,15 @@ w4a16_status_t w4a16_moe_layer_ex(const uint16_t* x, const w4a16_packed_weights_
   float* y = reinterpret_cast<float*>(ws + L.off_y);
   const int n_slots = T * top_k;
 
-  cudaError_t err = launch_moe_align(topk_ids, n_slots, E, L.block_m, sorted_ids, expert_ids, ntp,
-                                     L.cap, 0, dev_err,
-                                     reinterpret_cast<int32_t*>(ws + L.off_cnt),
-                                     static_cast<int>(split_unit_budget(L.block_m)), stream);
-  if (err != cudaSuccess) return cuda_fail(err, "moe_align launch");
+  // the align kernel also clears counters for the kernels after it: the K-split counters, or
+  // the single-kernel layer's block and phase counts
   int32_t* blk_done = reinterpret_cast<int32_t*>(ws + L.off_done);
-  if (one_kernel) {  // FP32 token sums and the per-block gate_up completion counts
-    err = launch_zero2(y, static_cast<int64_t>(T) * H, blk_done,
-                       static_cast<int64_t>(round_up(static_cast<size_t>(L.cap / L.block_m), 4)),
-                       dev.num_sms, stream);
-    if (err != cudaSuccess) return cuda_fail(err, "zero launch");
-  } else if (fused) {  // the down GEMM adds into FP32 token sums held where the per-slot rows would be
+  cudaError_t err = launch_moe_align(
+      topk_ids, n_slots, E, L.block_m, sorted_ids, expert_ids, ntp, L.cap, 0, dev_err,
+      one_kernel ? blk_done : reinterpret_cast<int32_t*>(ws + L.off_cnt),
+      static_cast<int>(one_kernel ? done_words(L) : split_unit_budget(L.block_m)), stream);
+  if (err != cudaSuccess) return cuda_fail(err, "moe_align launch");
+  if (!one_kernel && fused) {  // the down GEMM adds into FP32 token sums held where the per-slot rows would be
     err = launch_zero_f32(y, static_cast<int64_t>(T) * H, dev.num_sms, stream);
     if (err != cudaSuccess) return cuda_fail(err, "zero launch");
   }
@@ -840,16 +824,21 @@ w4a16_status_t w4a16_moe_layer_ex(const uint16_t* x, const w4a16_packed_weights_
     bool empty1 = false, empty2 = false;
     if ((st = prepare_gemm(g1, dev, &a1, &grid1, &empty1)) != W4A16_OK) return st;
     if ((st = prepare_gemm(g2, dev, &a2, &grid2, &empty2)) != W4A16_OK) return st;
-    if (!empty1 && !empty2) {
-      a1.signal_done = blk_done;
-      a2.wait_done = blk_done;
-      a2.wait_count = a1.n_tiles;
-      a2.routing_ready = a1.routing_ready;
-      err = launch_layer_fused(a1, a2, dev.num_sms, stream);
-      if (err != cudaSuccess) return cuda_fail(err, "fused layer launch");
+    if (empty1 || empty2) {  // nothing routed: the output is zeros
+      err = cudaMemsetAsync(out, 0, static_cast<size_t>(T) * H * sizeof(uint16_t), stream);
+      if (err != cudaSuccess) return cuda_fail(err, "output clear");
+      return W4A16_OK;
     }
-    err = launch_round_bf16(y, static_cast<int64_t>(T) * H, out, dev.num_sms, stream);
-    if (err != cudaSuccess) return cuda_fail(err, "round launch");
+    a1.signal_done = blk_done;
+    a2.wait_done = blk_done;
+    a2.wait_count = a1.n_tiles;
+    a2.routing_ready = a1.routing_ready;
+    // the kernel zeroes the sums, merges into them and rounds them into out
+    a2.sync = blk_done + L.cap / L.block_m;
+    a2.sum_elems = static_cast<int64_t>(T) * H;
+    a2.final_out = out;
+    err = launch_layer_fused(a1, a2, dev.num_sms, stream);
+    if (err != cudaSuccess) return cuda_fail(err, "fused layer launch");
     return W4A16_OK;
   }
   if ((st = run_gemm(g1, dev, stream)) != W4A16_OK) return st;

@@ -679,6 +679,17 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
     const int t = q * 32 + lane;  // tile row = TMEM lane
     uint8_t* epi_stage = epi_stage_base + q * kEpiStageBytes;
     uint32_t lu = 0;
+    // single-kernel layer: zero this CTA's slice of the FP32 token sums, then count it
+    bool sums_zeroed = !(FUSED && a2.sync);
+    if (FUSED && a2.sync) {
+      float4* sums = reinterpret_cast<float4*>(a2.C);
+      const int64_t n4 = a2.sum_elems / 4;
+      for (int64_t i = static_cast<int64_t>(blockIdx.x) * 128 + t; i < n4;
+           i += static_cast<int64_t>(gridDim.x) * 128)
+        sums[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      named_bar_epi();
+      if (t == 0) red_release_add(a2.sync, 1);
+    }
     for (int64_t u = PAIR ? unit0 : blockIdx.x; u < n_units; u += PAIR ? ustride : gridDim.x) {
       const Unit un = decode_any<FUSED, PAIR>(a, a2, split_k, units0_u, crank, u);
       if (!un.ok) continue;
@@ -690,6 +701,12 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       const uint32_t pab = (lu >> 1) & 1;
       const bool ok = wait_bar<PAIR>(smem_u32(&accfull[ab]), pab, abort_flag, a.dev_err);
       if (epi_any(!ok)) break;
+      if (FUSED && g.sync && !sums_zeroed) {
+        // the first merge of this CTA: every CTA's slice of the sums must be zero
+        if (t == 0) wait_count_at_least(g.sync, static_cast<int32_t>(gridDim.x), abort_flag, g.dev_err);
+        named_bar_epi();
+        sums_zeroed = true;
+      }
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ab * NT;
       if (split_k == 1) {
@@ -766,6 +783,29 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
         if (t == 0) red_release_add(g.signal_done + un.b, 1);
       }
       ++lu;
+    }
+    if (FUSED && a2.sync && a2.final_out) {
+      // every CTA's merges are done: round this CTA's slice of the sums to BF16
+      named_bar_epi();
+      if (t == 0) {
+        red_release_add(a2.sync + 1, 1);
+        wait_count_at_least(a2.sync + 1, static_cast<int32_t>(gridDim.x), abort_flag, a2.dev_err);
+      }
+      named_bar_epi();
+      if (!*abort_flag) {
+        const float4* sums = reinterpret_cast<const float4*>(a2.C);
+        uint4* out = reinterpret_cast<uint4*>(a2.final_out);
+        const int64_t n8 = a2.sum_elems / 8;
+        for (int64_t i = static_cast<int64_t>(blockIdx.x) * 128 + t; i < n8;
+             i += static_cast<int64_t>(gridDim.x) * 128) {
+          const float4 x = __ldcg(sums + 2 * i), y = __ldcg(sums + 2 * i + 1);
+          auto pk = [](float lo, float hi) {
+            return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+                   (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+          };
+          out[i] = make_uint4(pk(x.x, x.y), pk(x.z, x.w), pk(y.x, y.y), pk(y.z, y.w));
+        }
+      }
     }
   } else if (warp >= 8) {
     // ---------------- dequant warpgroups (stages rotate over the groups) ----------------

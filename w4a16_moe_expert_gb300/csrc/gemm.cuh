@@ -45,6 +45,12 @@ struct GemmArgs {
   int32_t* signal_done;
   const int32_t* wait_done;
   int wait_count;
+  // single-kernel layer, down GEMM only: sync[0] counts CTAs that zeroed their slice of the
+  // FP32 token sums C (sum_elems floats), sync[1] CTAs whose units are all done; the last
+  // phase rounds the sums into final_out (BF16)
+  int32_t* sync;
+  int64_t sum_elems;
+  uint16_t* final_out;
   // CTA pairs (block_m 128): units are (block, pair of 128-row tiles); divisor n_tiles / 2
   int pair;
   uint32_t nt2_magic, nt2_shift;
