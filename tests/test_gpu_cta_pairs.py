@@ -1,6 +1,8 @@
-"""CTA pairs (tcgen05 cta_group::2: one M = 256 MMA over two CTAs' 128-row weight tiles, each
-CTA holding half of a 128-token block's activation rows) against the CPU oracle and against
-the one-CTA schedule, through the C ABI."""
+"""CTA pairs against the CPU oracle and against the one-CTA schedule, through the C ABI: mode 2
+(tcgen05 cta_group::2: one M = 256 MMA over two CTAs' 128-row weight tiles, each CTA holding
+half of a 128-token block's activation rows) and mode 3 (two-CTA clusters on the two tiles of a
+pair, each CTA with its own MMAs, the block's activation tiles loaded once for both by
+multicast TMA)."""
 from __future__ import annotations
 
 import pytest
@@ -12,6 +14,7 @@ from w4a16_moe_expert_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
+MODES = [2, 3]
 
 
 @pytest.fixture(scope="module")
@@ -30,13 +33,14 @@ def _case(lib, T, k, E, N, K, seed, paired=False):
     return qw, sc, x, ids, W, r, xs, (s, e, ntp)
 
 
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("paired,epilogue", [(False, 0), (True, 0), (True, 1)])
-def test_pairs_match_oracle_and_single_cta(lib, paired, epilogue):
+def test_pairs_match_oracle_and_single_cta(lib, mode, paired, epilogue):
     T, k, E, N, K = 200, 4, 6, 512, 384
     qw, sc, x, ids, W, r, xs, (s, e, ntp) = _case(lib, T, k, E, N, K, 51, paired)
     kw = dict(epilogue=epilogue, row_flags=lib.A_ROWS_SORTED)
     one = lib.moe_gemm(xs, 1, W, r, cta_pairs=1, **kw).cpu()
-    two = lib.moe_gemm(xs, 1, W, r, cta_pairs=2, **kw).cpu()
+    two = lib.moe_gemm(xs, 1, W, r, cta_pairs=mode, **kw).cpu()
     ref = oracle.moe_gemm(x, k, qw, sc, s, e, ntp, 128, T * k)
     if epilogue:
         ref = oracle.silu_mul(ref)
@@ -46,18 +50,20 @@ def test_pairs_match_oracle_and_single_cta(lib, paired, epilogue):
     assert torch.equal(bits(two[rows]), bits(one[rows]))
 
 
-def test_pairs_fp32_rows_and_grid_sizes(lib):
+@pytest.mark.parametrize("mode", MODES)
+def test_pairs_fp32_rows_and_grid_sizes(lib, mode):
     T, k, E, N, K = 300, 8, 16, 768, 256
     qw, sc, x, ids, W, r, xs, (s, e, ntp) = _case(lib, T, k, E, N, K, 52)
     base = lib.moe_gemm(xs, 1, W, r, row_flags=lib.A_ROWS_SORTED | lib.C_FP32, cta_pairs=1).cpu()
     rows = routed_rows(ids)
     for ctas in (2, 6, 64, 152):
-        got = lib.moe_gemm(xs, 1, W, r, row_flags=lib.A_ROWS_SORTED | lib.C_FP32, cta_pairs=2,
+        got = lib.moe_gemm(xs, 1, W, r, row_flags=lib.A_ROWS_SORTED | lib.C_FP32, cta_pairs=mode,
                            num_ctas=ctas).cpu()
         assert torch.equal(got[rows].view(torch.int32), base[rows].view(torch.int32)), f"grid {ctas}"
 
 
-def test_pairs_one_hot_reads_weights_back_exactly(lib):
+@pytest.mark.parametrize("mode", MODES)
+def test_pairs_one_hot_reads_weights_back_exactly(lib, mode):
     E, N, K = 2, 256, 128
     qw, sc = workloads.draw_weights(E, N, K, seed=53)
     W = lib.pack_weights(qw.to(DEV), sc.to(DEV))
@@ -67,11 +73,12 @@ def test_pairs_one_hot_reads_weights_back_exactly(lib):
         ids = torch.full((K, 1), ex, dtype=torch.int32)
         r = lib.moe_align(ids.to(DEV), E, 128)
         xs = lib.gather_rows(x.to(DEV), 1, r)
-        C = lib.moe_gemm(xs, 1, W, r, row_flags=lib.A_ROWS_SORTED, cta_pairs=2).cpu()
+        C = lib.moe_gemm(xs, 1, W, r, row_flags=lib.A_ROWS_SORTED, cta_pairs=mode).cpu()
         assert torch.equal(bits(C), bits(ref[ex].T.contiguous())), f"expert {ex}"
 
 
-def test_pairs_qwen3_prefill_sampled_rows(lib):
+@pytest.mark.parametrize("mode", MODES)
+def test_pairs_qwen3_prefill_sampled_rows(lib, mode):
     wl = workloads.WORKLOADS["qwen3_30b_a3b"]
     T = 4096
     qw, sc = workloads.draw_weights(wl.E, 2 * wl.I, wl.H, seed=54)
@@ -82,15 +89,16 @@ def test_pairs_qwen3_prefill_sampled_rows(lib):
     xs = lib.gather_rows(x.to(DEV), wl.top_k, r)
     s, e, ntp = oracle.moe_align(ids, wl.E, 128)
     C = lib.moe_gemm(xs, 1, W, r, epilogue=1, row_flags=lib.A_ROWS_SORTED | lib.C_ROWS_SORTED,
-                     cta_pairs=2).cpu()
+                     cta_pairs=mode).cpu()
     pos = torch.nonzero(torch.from_numpy(s[:ntp]) < T * wl.top_k).reshape(-1)[::97]
     slots = torch.from_numpy(s[pos.numpy()]).long()
     experts = torch.from_numpy(e[(pos // 128).numpy()]).long()
     ref = oracle.silu_mul(oracle.gemm_rows(x, wl.top_k, qw, sc, slots.numpy(), experts.numpy()))
-    assert_close_bf16(C[pos], ref, "qwen3 T=4096 pairs")
+    assert_close_bf16(C[pos], ref, f"qwen3 T=4096 pairs mode {mode}")
 
 
-def test_pairs_rejected_where_they_cannot_run(lib):
+@pytest.mark.parametrize("mode", MODES)
+def test_pairs_rejected_where_they_cannot_run(lib, mode):
     E, N, K = 4, 256, 128
     qw, sc = workloads.draw_weights(E, N, K, seed=55)
     W = lib.pack_weights(qw.to(DEV), sc.to(DEV))
@@ -98,10 +106,10 @@ def test_pairs_rejected_where_they_cannot_run(lib):
     ids, _ = workloads.draw_routing(20, E, 2, seed=55)
     r64 = lib.moe_align(ids.to(DEV), E, 64)
     with pytest.raises(lib.LibraryError, match="invalid argument"):
-        lib.moe_gemm(x.to(DEV), 2, W, r64, cta_pairs=2)  # 64-token blocks, gathered rows
+        lib.moe_gemm(x.to(DEV), 2, W, r64, cta_pairs=mode)  # 64-token blocks, gathered rows
     r = lib.moe_align(ids.to(DEV), E, 128)
     with pytest.raises(lib.LibraryError, match="invalid argument"):
-        lib.moe_gemm(x.to(DEV), 2, W, r, cta_pairs=2)  # rows not in sorted order
+        lib.moe_gemm(x.to(DEV), 2, W, r, cta_pairs=mode)  # rows not in sorted order
     xs = lib.gather_rows(x.to(DEV), 2, r)
     with pytest.raises(lib.LibraryError, match="invalid argument"):
-        lib.moe_gemm(xs, 1, W, r, row_flags=lib.A_ROWS_SORTED, cta_pairs=2, split_k=2)
+        lib.moe_gemm(xs, 1, W, r, row_flags=lib.A_ROWS_SORTED, cta_pairs=mode, split_k=2)

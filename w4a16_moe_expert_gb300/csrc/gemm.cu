@@ -326,9 +326,14 @@ __device__ __forceinline__ void arrive_handoff(uint32_t bar, bool leader, int la
   }
 }
 
-template <int NT, int KS, bool FUSED, bool PAIR = false>
+template <int NT, int KS, bool FUSED, bool PAIR = false, bool MC = false>
 __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2) {
   using Cfg = GemmCfg<NT, KS, PAIR>;
+  // CL: two-CTA clusters taking the two tiles of a tile pair of one block.  PAIR: one
+  // cta_group::2 MMA over both CTAs.  MC: each CTA runs its own MMAs; the block's activation
+  // tiles are loaded once for both CTAs (multicast TMA, each CTA issuing half of the K
+  // sub-blocks), and an activation slot is free once both CTAs' MMAs have read it.
+  constexpr bool CL = PAIR || MC;
   constexpr int S_W = Cfg::kWStages;
   constexpr int S_B = Cfg::kBStages;
   constexpr int S_A = Cfg::kAStages;
@@ -361,10 +366,10 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // CTA pairs: the even CTA of each two-CTA cluster issues the MMAs; the odd one forwards its
   // activation tiles' arrival and its dequant / epilogue hand-offs to the even CTA's barriers
-  const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
+  const uint32_t crank = CL ? cluster_ctarank() : 0u;
   const bool leader = crank == 0;
-  const int64_t unit0 = PAIR ? (blockIdx.x >> 1) : blockIdx.x;
-  const int64_t ustride = PAIR ? (gridDim.x >> 1) : gridDim.x;
+  const int64_t unit0 = CL ? (blockIdx.x >> 1) : blockIdx.x;
+  const int64_t ustride = CL ? (gridDim.x >> 1) : gridDim.x;
   const bool gather = !a.a_sorted;
   // a fused call may mix gathered and TMA-loaded activations (one GEMM each): every stage then
   // completes on 64 arrivals, the TMA path's lane 0 also expecting the tile's bytes
@@ -377,7 +382,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
     }
     for (int s = 0; s < S_B; ++s) {
       mbar_init(smem_u32(&bfull[s]), PAIR ? (leader ? 2 : 1) : ((FUSED || gather) ? kGatherThreads : 1));
-      mbar_init(smem_u32(&bempty[s]), 1);
+      mbar_init(smem_u32(&bempty[s]), MC ? 2 : 1);  // MC: both CTAs' commits
     }
     for (int s = 0; s < S_A; ++s) {
       mbar_init(smem_u32(&afull[s]), PAIR ? 8 : 128);  // pairs: one arrival per warp of both CTAs
@@ -409,7 +414,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
   }
   tc_fence_before();
   __syncthreads();
-  if (PAIR) cluster_sync();  // both CTAs' barriers exist before either arrives on the other's
+  if (CL) cluster_sync();  // both CTAs' barriers exist before either arrives on the other's
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -425,7 +430,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
   // Fewer K splits when the routed blocks would overflow the partial-sum scratch.
   int split_k = a.split_k;
   while (split_k > 1 && nblocks * a.n_tiles * split_k > a.max_split_units) --split_k;
-  const int64_t units0 = PAIR ? nblocks * (a.n_tiles >> 1) : nblocks * a.n_tiles * split_k;
+  const int64_t units0 = CL ? nblocks * (a.n_tiles >> 1) : nblocks * a.n_tiles * split_k;
   const int64_t n_units = FUSED ? units0 + nblocks * a2.n_tiles : units0;
   const uint32_t units0_u = static_cast<uint32_t>(units0);
 
@@ -436,8 +441,8 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
     // Weights never depend on the previous kernel, so they stream before pdl_wait.
     const uint64_t policy = a.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
     uint32_t it = 0;
-    for (int64_t u = PAIR ? unit0 : blockIdx.x; u < n_units; u += PAIR ? ustride : gridDim.x) {
-      const Unit un = decode_any<FUSED, PAIR>(a, a2, split_k, units0_u, crank, u);
+    for (int64_t u = CL ? unit0 : blockIdx.x; u < n_units; u += CL ? ustride : gridDim.x) {
+      const Unit un = decode_any<FUSED, CL>(a, a2, split_k, units0_u, crank, u);
       if (!un.ok) continue;
       const GemmArgs& g = args_of<FUSED>(a, a2, un);
       const uint8_t* strip = g.wblob + kHeaderBytes +
@@ -471,8 +476,8 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       const int gt = tid - 64;
       const int c = gt & 7;
       constexpr int R = NT / 8;
-      for (int64_t u = PAIR ? unit0 : blockIdx.x; u < n_units; u += PAIR ? ustride : gridDim.x) {
-        const Unit un = decode_any<FUSED, PAIR>(a, a2, split_k, units0_u, crank, u);
+      for (int64_t u = CL ? unit0 : blockIdx.x; u < n_units; u += CL ? ustride : gridDim.x) {
+        const Unit un = decode_any<FUSED, CL>(a, a2, split_k, units0_u, crank, u);
         if (!un.ok) continue;
         const GemmArgs& g = args_of<FUSED>(a, a2, un);
         if (g.wait_done) {
@@ -536,8 +541,8 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       const int g = tid - 64;
       const int c = g & 7;  // 16-byte chunk of a 128-byte row handled by this thread
       constexpr int R = NT / 8;  // rows per thread: (g >> 3) + 8j
-      for (int64_t u = PAIR ? unit0 : blockIdx.x; u < n_units; u += PAIR ? ustride : gridDim.x) {
-        const Unit un = decode_any<FUSED, PAIR>(a, a2, split_k, units0_u, crank, u);
+      for (int64_t u = CL ? unit0 : blockIdx.x; u < n_units; u += CL ? ustride : gridDim.x) {
+        const Unit un = decode_any<FUSED, CL>(a, a2, split_k, units0_u, crank, u);
         if (!un.ok) continue;
         int32_t arow[R];
 #pragma unroll
@@ -569,8 +574,8 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       cp_async_wait_all();
     } else if (warp == 2) {
       // rows already in sorted order: one 2-D TMA tile per K sub-block, rotating lanes
-      for (int64_t u = PAIR ? unit0 : blockIdx.x; u < n_units; u += PAIR ? ustride : gridDim.x) {
-        const Unit un = decode_any<FUSED, PAIR>(a, a2, split_k, units0_u, crank, u);
+      for (int64_t u = CL ? unit0 : blockIdx.x; u < n_units; u += CL ? ustride : gridDim.x) {
+        const Unit un = decode_any<FUSED, CL>(a, a2, split_k, units0_u, crank, u);
         if (!un.ok) continue;
         for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
           const int nsub = min(KS, un.kb1 - kb);
@@ -579,13 +584,19 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
           if (!__all_sync(0xffffffffu, wait_bar<PAIR>(smem_u32(&bempty[s]), ph ^ 1, abort_flag, a.dev_err)))
             goto tprod_done;
           const uint32_t bb = smem_u32(&bfull[s]);
-          if (lane == 0) mbar_arrive_expect_tx(bb, nsub * Cfg::kSubB);
+          if (lane == 0) mbar_arrive_expect_tx(bb, nsub * Cfg::kSubB);  // MC: both CTAs' halves
           __syncwarp();
-          for (int sb = 0; sb < nsub; ++sb)
-            if (lane == static_cast<int>((it * KS + sb) & 31))
-              tma_load_2d(smem_u32(b_ring + s * Cfg::kBBytes + sb * Cfg::kSubB), &a.tmap_a,
-                          (kb + sb) * kBlockK,
+          for (int sb = 0; sb < nsub; ++sb) {
+            if (lane != static_cast<int>((it * KS + sb) & 31)) continue;
+            const uint32_t dst = smem_u32(b_ring + s * Cfg::kBBytes + sb * Cfg::kSubB);
+            if (MC) {
+              if ((sb & 1) == static_cast<int>(crank))
+                tma_load_2d_mc2(dst, &a.tmap_a, (kb + sb) * kBlockK, static_cast<int>(un.b * a.block_m), bb);
+            } else {
+              tma_load_2d(dst, &a.tmap_a, (kb + sb) * kBlockK,
                           static_cast<int>(un.b * a.block_m + (PAIR ? crank * (NT / 2) : 0)), bb);
+            }
+          }
           __syncwarp();
         }
       }
@@ -604,8 +615,8 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       // then wait for the pair's last MMAs before the TMEM they write is released
       if (elect_one()) {
         uint32_t it = 0;
-        for (int64_t u = PAIR ? unit0 : blockIdx.x; u < n_units; u += PAIR ? ustride : gridDim.x) {
-          const Unit un = decode_any<FUSED, PAIR>(a, a2, split_k, units0_u, crank, u);
+        for (int64_t u = CL ? unit0 : blockIdx.x; u < n_units; u += CL ? ustride : gridDim.x) {
+          const Unit un = decode_any<FUSED, CL>(a, a2, split_k, units0_u, crank, u);
           if (!un.ok) continue;
           for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
             const int sbi = it % S_B;
@@ -619,8 +630,8 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       }
     } else if (elect_one()) {
       uint32_t it = 0, lu = 0;
-      for (int64_t u = PAIR ? unit0 : blockIdx.x; u < n_units; u += PAIR ? ustride : gridDim.x) {
-        const Unit un = decode_any<FUSED, PAIR>(a, a2, split_k, units0_u, crank, u);
+      for (int64_t u = CL ? unit0 : blockIdx.x; u < n_units; u += CL ? ustride : gridDim.x) {
+        const Unit un = decode_any<FUSED, CL>(a, a2, split_k, units0_u, crank, u);
         if (!un.ok) continue;
         const bool rows_gathered = FUSED ? !args_of<FUSED>(a, a2, un).a_sorted : gather;
         const int ab = lu & 1;
@@ -644,7 +655,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
           if (rows_gathered) fence_proxy_async_smem();  // cp.async (generic proxy) rows -> tensor core
           tc_fence_after();
           if (prev_sbi >= 0) {
-            commit_any<PAIR>(smem_u32(&bempty[prev_sbi]));
+            if (MC) mma_commit_mc2(smem_u32(&bempty[prev_sbi])); else commit_any<PAIR>(smem_u32(&bempty[prev_sbi]));
             commit_any<PAIR>(smem_u32(&aempty[prev_sa]));
           }
           const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((sbi * Cfg::kBBytes) >> 4);
@@ -674,7 +685,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
           prev_sa = sa;
         }
         if (prev_sbi >= 0) {
-          commit_any<PAIR>(smem_u32(&bempty[prev_sbi]));
+          if (MC) mma_commit_mc2(smem_u32(&bempty[prev_sbi])); else commit_any<PAIR>(smem_u32(&bempty[prev_sbi]));
           commit_any<PAIR>(smem_u32(&aempty[prev_sa]));
         }
         commit_any<PAIR>(smem_u32(&accfull[ab]));
@@ -683,6 +694,12 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
     mma_done:
       commit_any<PAIR>(smem_u32(drain));
       wait_bar_plain<PAIR>(smem_u32(drain), 0);
+      if (MC) {
+        // the peer's commits to this CTA's activation slots must all have landed before
+        // either CTA of the cluster exits: wait for the last release of every slot
+        for (uint32_t j = (it > static_cast<uint32_t>(S_B) ? it - S_B : 0); j < it; ++j)
+          wait_bar_plain<false>(smem_u32(&bempty[j % S_B]), (j / S_B) & 1);
+      }
     }
     __syncwarp();
   } else if (warp >= 4 && warp < 8) {
@@ -703,8 +720,8 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       named_bar_epi();
       if (t == 0) red_release_add(a2.sync, 1);
     }
-    for (int64_t u = PAIR ? unit0 : blockIdx.x; u < n_units; u += PAIR ? ustride : gridDim.x) {
-      const Unit un = decode_any<FUSED, PAIR>(a, a2, split_k, units0_u, crank, u);
+    for (int64_t u = CL ? unit0 : blockIdx.x; u < n_units; u += CL ? ustride : gridDim.x) {
+      const Unit un = decode_any<FUSED, CL>(a, a2, split_k, units0_u, crank, u);
       if (!un.ok) continue;
       const GemmArgs& g = args_of<FUSED>(a, a2, un);
       named_bar_epi();  // the previous unit's readers of epi_rows / last_flag are done
@@ -827,8 +844,8 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
     const int t = q * 32 + lane;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + Cfg::kACol0;
     uint32_t it = 0;
-    for (int64_t u = PAIR ? unit0 : blockIdx.x; u < n_units; u += PAIR ? ustride : gridDim.x) {
-      const Unit un = decode_any<FUSED, PAIR>(a, a2, split_k, units0_u, crank, u);
+    for (int64_t u = CL ? unit0 : blockIdx.x; u < n_units; u += CL ? ustride : gridDim.x) {
+      const Unit un = decode_any<FUSED, CL>(a, a2, split_k, units0_u, crank, u);
       if (!un.ok) continue;
       // the tile's INT4 conversion (uniform over the unit, read while the weights are in flight)
       const GemmArgs& ga = args_of<FUSED>(a, a2, un);
@@ -909,7 +926,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
   }
   tc_fence_before();
   __syncthreads();
-  if (PAIR) cluster_sync();  // the peer is done with the pair's TMEM and barriers
+  if (CL) cluster_sync();  // the peer is done with the pair's TMEM and barriers
   if (warp == 1) {
     tc_fence_after();
     if (PAIR) tmem_dealloc_pair(tmem_base, kTmemCols); else tmem_dealloc(tmem_base, kTmemCols);
@@ -928,6 +945,14 @@ template <int NT, int KS>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_pair_kernel(const __grid_constant__ GemmArgs a) {
   gemm_body<NT, KS, false, true>(a, a);
+}
+
+// Multicast pairs (128-token blocks): two-CTA clusters, one 128-row tile each, the block's
+// activation tiles loaded once for both.
+template <int NT, int KS>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    moe_gemm_mc_kernel(const __grid_constant__ GemmArgs a) {
+  gemm_body<NT, KS, false, false, true>(a, a);
 }
 
 // Fused layer: the gate_up GEMM (a, SiLU-and-mul into sorted rows) and the down GEMM (a2, rows
@@ -1109,13 +1134,14 @@ cudaError_t launch_layer_fused(GemmArgs& a, GemmArgs& a2, int grid, cudaStream_t
   }
 }
 
+template <bool MC>
 static cudaError_t launch_gemm_pair(GemmArgs& args, int grid, bool pdl, cudaStream_t stream) {
   constexpr int NT = 128, KS = StageK<NT>::value;
-  using Cfg = GemmCfg<NT, KS, true>;
+  using Cfg = GemmCfg<NT, KS, !MC>;
+  auto kernel = MC ? moe_gemm_mc_kernel<NT, KS> : moe_gemm_pair_kernel<NT, KS>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t err = cudaFuncSetAttribute(moe_gemm_pair_kernel<NT, KS>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(Cfg::kSmemBytes));
     if (err != cudaSuccess) return err;
     configured = true;
@@ -1134,17 +1160,19 @@ static cudaError_t launch_gemm_pair(GemmArgs& args, int grid, bool pdl, cudaStre
   attr[1].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, moe_gemm_pair_kernel<NT, KS>, args);
+  return cudaLaunchKernelEx(&cfg, kernel, args);
 }
 
 cudaError_t launch_gemm(GemmArgs& args, int grid, bool pdl, cudaStream_t stream) {
   if (args.pair) {  // block_m 128, sorted rows, even tile count, no K split (checked by the caller)
     if (args.block_m != 128 || !args.a_sorted || args.split_k != 1 || args.n_tiles % 2 || grid < 2)
       return cudaErrorInvalidValue;
+    const bool mc = args.pair == 2;
     cudaError_t err = make_act_tmap(&args.tmap_a, args.A, args.capacity, args.K, args.lda,
-                                    args.block_m / 2);
+                                    mc ? args.block_m : args.block_m / 2);
     if (err != cudaSuccess) return err;
-    return launch_gemm_pair(args, grid, pdl, stream);
+    return mc ? launch_gemm_pair<true>(args, grid, pdl, stream)
+              : launch_gemm_pair<false>(args, grid, pdl, stream);
   }
   const int64_t rows = args.a_sorted
                            ? args.capacity
