@@ -50,7 +50,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 ROOFLINE_T = 64
 # Its DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum from an ncu capture
 # of that launch), valid only while the GEMM kernel's sources hash to the recorded value.
-ROOFLINE_TRAFFIC = {"sources_sha256": "7968a2d89d202a6414cb78816a23be72e0bd5b3d105327e3956693c29d579eec", "bytes": 223303168 + 3685632}
+ROOFLINE_TRAFFIC = {"sources_sha256": "d1663ade3e8d9a10813e3c80b28831e065f05b1ce842d41bc7dd5f67b35b1be6", "bytes": 223305984 + 3692800}
 GEMM_SOURCES = ("w4a16_moe_expert_gb300/csrc/gemm.cu", "w4a16_moe_expert_gb300/csrc/gemm.cuh",
                 "w4a16_moe_expert_gb300/csrc/common.cuh")
 
@@ -483,22 +483,30 @@ def run_ours(args, rank, world, local_rank):
                 "weight_GBps": round(small["acct"]["gate_up"]["weight_bytes"] / t_m / 1e3, 1)}
         extras["grouped_contracts"] = grouped
 
-        # CTA pairs (tcgen05 cta_group::2, M = 256) on the 128-token-block calls, same method
+        # CTA pairs on the 128-token-block calls, same method: mode 2 (tcgen05 cta_group::2,
+        # M = 256) and mode 3 (two-CTA clusters sharing the activation tiles by multicast TMA)
         pair_rows = []
         for c in cases:
             if c["block_m"] != 128 or (2 * wl.I // 128) % 2 or (wl.H // 128) % 2:
                 continue
             r, hint = c["routing"], rows_hint[c["T"]]
-            gu = per_call_us(lambda i: (lib.gather_rows(c["x"], wl.top_k, r, out=c["xs"]), lib.moe_gemm(
-                c["xs"], 1, w13s[i % c["n_gu"]], r, epilogue=lib.EPILOGUE_SILU_MUL,
-                row_flags=lib.A_ROWS_SORTED | lib.C_ROWS_SORTED, out=c["h"], workspace=c["ws"],
-                expected_rows_per_expert=hint, cta_pairs=2)), c["R_gu"])
-            dn = per_call_us(lambda i: lib.moe_gemm(
-                c["h"], 1, w2s[i % c["n_dn"]], r, row_flags=lib.A_ROWS_SORTED | lib.C_FP32,
-                out=c["y"], workspace=c["ws"], expected_rows_per_expert=hint, cta_pairs=2), c["R_dn"])
-            pair_rows.append({"T": c["T"], "gate_up_us": round(gu, 2), "down_us": round(dn, 2)})
+            row = {"T": c["T"]}
+            for mode, key in ((2, "m256"), (3, "multicast")):
+                gu = per_call_us(lambda i: (lib.gather_rows(c["x"], wl.top_k, r, out=c["xs"]), lib.moe_gemm(
+                    c["xs"], 1, w13s[i % c["n_gu"]], r, epilogue=lib.EPILOGUE_SILU_MUL,
+                    row_flags=lib.A_ROWS_SORTED | lib.C_ROWS_SORTED, out=c["h"], workspace=c["ws"],
+                    expected_rows_per_expert=hint, cta_pairs=mode)), c["R_gu"])
+                dn = per_call_us(lambda i: lib.moe_gemm(
+                    c["h"], 1, w2s[i % c["n_dn"]], r, row_flags=lib.A_ROWS_SORTED | lib.C_FP32,
+                    out=c["y"], workspace=c["ws"], expected_rows_per_expert=hint, cta_pairs=mode),
+                    c["R_dn"])
+                row[f"{key}_gate_up_us"] = round(gu, 2)
+                row[f"{key}_down_us"] = round(dn, 2)
+            pair_rows.append(row)
         extras["cta_pairs"] = {
-            "what": "128-token-block calls with CTA pairs (one M=256 tcgen05 MMA over two CTAs' tiles)",
+            "what": "128-token-block calls with CTA pairs: m256 = one M=256 tcgen05 MMA over two "
+                    "CTAs' tiles; multicast = two-CTA clusters, one MMA stream each, activation "
+                    "tiles loaded once for both",
             "sweep": pair_rows}
 
     # e2e through the public layer call, host buffers, copies inside the timed region
