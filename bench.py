@@ -50,7 +50,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 ROOFLINE_T = 64
 # Its DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum from an ncu capture
 # of that launch), valid only while the GEMM kernel's sources hash to the recorded value.
-ROOFLINE_TRAFFIC = {"sources_sha256": "d1663ade3e8d9a10813e3c80b28831e065f05b1ce842d41bc7dd5f67b35b1be6", "bytes": 223305984 + 3692800}
+ROOFLINE_TRAFFIC = {"sources_sha256": "1fbe94770e0ba47003fdf8a266766394be73f5593de3ce28eaec54f53f00127b", "bytes": 223309312 + 3544576}
 GEMM_SOURCES = ("w4a16_moe_expert_gb300/csrc/gemm.cu", "w4a16_moe_expert_gb300/csrc/gemm.cuh",
                 "w4a16_moe_expert_gb300/csrc/common.cuh")
 
