@@ -51,6 +51,21 @@ def test_pairs_match_oracle_and_single_cta(lib, mode, paired, epilogue):
 
 
 @pytest.mark.parametrize("mode", MODES)
+def test_pairs_odd_k_tail(lib, mode):
+    # K = 448: seven 64-wide K blocks, so the last stage holds one (in multicast pairs only the
+    # even CTA loads it, for both)
+    T, k, E, N, K = 150, 4, 5, 512, 448
+    qw, sc, x, ids, W, r, xs, (s, e, ntp) = _case(lib, T, k, E, N, K, 56, True)
+    kw = dict(epilogue=1, row_flags=lib.A_ROWS_SORTED)
+    one = lib.moe_gemm(xs, 1, W, r, cta_pairs=1, **kw).cpu()
+    two = lib.moe_gemm(xs, 1, W, r, cta_pairs=mode, **kw).cpu()
+    ref = oracle.silu_mul(oracle.moe_gemm(x, k, qw, sc, s, e, ntp, 128, T * k))
+    rows = routed_rows(ids)
+    assert_close_bf16(two[rows], ref[rows], f"pairs mode {mode}, K tail")
+    assert torch.equal(bits(two[rows]), bits(one[rows]))
+
+
+@pytest.mark.parametrize("mode", MODES)
 def test_pairs_fp32_rows_and_grid_sizes(lib, mode):
     T, k, E, N, K = 300, 8, 16, 768, 256
     qw, sc, x, ids, W, r, xs, (s, e, ntp) = _case(lib, T, k, E, N, K, 52)
