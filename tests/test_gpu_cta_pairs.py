@@ -113,6 +113,21 @@ def test_pairs_qwen3_prefill_sampled_rows(lib, mode):
 
 
 @pytest.mark.parametrize("mode", MODES)
+def test_pairs_with_nothing_routed(lib, mode):
+    # every slot dropped: no block to compute, the output stays as it was
+    E, N, K, T, k = 4, 256, 128, 40, 2
+    qw, sc = workloads.draw_weights(E, N, K, seed=57)
+    W = lib.pack_weights(qw.to(DEV), sc.to(DEV))
+    ids = torch.full((T, k), -1, dtype=torch.int32)
+    r = lib.moe_align(ids.to(DEV), E, 128)
+    xs = torch.zeros((r.capacity, K), dtype=torch.bfloat16, device=DEV)
+    out = torch.full((T * k, N), 7.0, dtype=torch.float32, device=DEV)
+    lib.moe_gemm(xs, 1, W, r, row_flags=lib.A_ROWS_SORTED | lib.C_FP32, out=out, cta_pairs=mode)
+    assert int(r.num_tokens_padded.item()) == 0
+    assert torch.all(out.cpu() == 7.0)
+
+
+@pytest.mark.parametrize("mode", MODES)
 def test_pairs_rejected_where_they_cannot_run(lib, mode):
     E, N, K = 4, 256, 128
     qw, sc = workloads.draw_weights(E, N, K, seed=55)
