@@ -16,9 +16,15 @@ One step covers every T of the sweep:
 value = weight HBM GB/s over the sweep: sum of the packed weight bytes the two
 projections must read (experts with at least one routed row) divided by the sum
 of the per-call gate_up and down times (medians over the steps).  The roofline
-object describes the GEMM kernel (both projections): algorithmic bytes (weights +
-activations in + outputs) per call over its per-call time, against the measured
-HBM copy peak.
+object describes one launch, the decode-shape gate_up GEMM at T = 64: its
+algorithmic bytes (weights + activations in + outputs) over its per-call time,
+against the measured HBM copy peak, with its DRAM traffic from an ncu capture of
+the same sources; it also carries the sweep aggregate over all ten GEMM launches.
+e2e times the public layer call with pinned host inputs copied in and the output
+copied back inside the timed region.  config also reports per-T layer times in
+three modes (separate kernels, top-k merge in the down epilogue, one GEMM kernel),
+and unless --no-extras the sweep with NVFP4 weights, the grouped contracts and
+both kinds of CTA pairs at 128-token blocks.
 
 --impl reference times the CPU oracle (single-threaded C++) on a bounded sample
 of the same workload and reports the same metric.
