@@ -489,15 +489,14 @@ def run_ours(args, rank, world, local_rank):
                 "weight_GBps": round(small["acct"]["gate_up"]["weight_bytes"] / t_m / 1e3, 1)}
         extras["grouped_contracts"] = grouped
 
-        # CTA pairs on the 128-token-block calls, same method: mode 2 (tcgen05 cta_group::2,
-        # M = 256) and mode 3 (two-CTA clusters sharing the activation tiles by multicast TMA)
+        # CTA pairs on the 128-token-block calls, same method: tcgen05 cta_group::2, M = 256
         pair_rows = []
         for c in cases:
             if c["block_m"] != 128 or (2 * wl.I // 128) % 2 or (wl.H // 128) % 2:
                 continue
             r, hint = c["routing"], rows_hint[c["T"]]
             row = {"T": c["T"]}
-            for mode, key in ((2, "m256"), (3, "multicast")):
+            for mode, key in ((2, "m256"),):
                 gu = per_call_us(lambda i: (lib.gather_rows(c["x"], wl.top_k, r, out=c["xs"]), lib.moe_gemm(
                     c["xs"], 1, w13s[i % c["n_gu"]], r, epilogue=lib.EPILOGUE_SILU_MUL,
                     row_flags=lib.A_ROWS_SORTED | lib.C_ROWS_SORTED, out=c["h"], workspace=c["ws"],
@@ -511,8 +510,7 @@ def run_ours(args, rank, world, local_rank):
             pair_rows.append(row)
         extras["cta_pairs"] = {
             "what": "128-token-block calls with CTA pairs: m256 = one M=256 tcgen05 MMA over two "
-                    "CTAs' tiles; multicast = two-CTA clusters, one MMA stream each, activation "
-                    "tiles loaded once for both",
+                    "CTAs' tiles",
             "sweep": pair_rows}
 
     # e2e through the public layer call, host buffers, copies inside the timed region

@@ -186,11 +186,8 @@ typedef struct {
   int32_t split_k;   /* K slices per tile (1..16) */
   int32_t num_ctas;  /* persistent CTAs */
   int32_t cta_pairs; /* 128-token blocks only: 1 = one CTA per MMA, 2 = CTA pairs (tcgen05
-                        cta_group::2, M = 256 over two 128-row tiles), 3 = multicast pairs
-                        (two-CTA clusters on the two tiles of a pair, each CTA with its own
-                        MMAs, the block's activation tiles loaded once for both by multicast
-                        TMA); 2 and 3 need sorted activation rows, an even tile count and no K
-                        split; 0 = planner */
+                        cta_group::2, M = 256 over two 128-row tiles; needs sorted activation
+                        rows, an even tile count and no K split); 0 = planner */
 } w4a16_schedule_t;
 
 size_t w4a16_gemm_workspace_size(int total_slots, int E, int N, int K, int block_m);

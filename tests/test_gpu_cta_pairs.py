@@ -1,8 +1,6 @@
 """CTA pairs against the CPU oracle and against the one-CTA schedule, through the C ABI: mode 2
 (tcgen05 cta_group::2: one M = 256 MMA over two CTAs' 128-row weight tiles, each CTA holding
-half of a 128-token block's activation rows) and mode 3 (two-CTA clusters on the two tiles of a
-pair, each CTA with its own MMAs, the block's activation tiles loaded once for both by
-multicast TMA)."""
+half of a 128-token block's activation rows)."""
 from __future__ import annotations
 
 import pytest
@@ -14,7 +12,7 @@ from w4a16_moe_expert_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-MODES = [2, 3]
+MODES = [2]
 
 
 @pytest.fixture(scope="module")
@@ -52,8 +50,7 @@ def test_pairs_match_oracle_and_single_cta(lib, mode, paired, epilogue):
 
 @pytest.mark.parametrize("mode", MODES)
 def test_pairs_odd_k_tail(lib, mode):
-    # K = 448: seven 64-wide K blocks, so the last stage holds one (in multicast pairs only the
-    # even CTA loads it, for both)
+    # K = 448: seven 64-wide K blocks, so the last stage holds one
     T, k, E, N, K = 150, 4, 5, 512, 448
     qw, sc, x, ids, W, r, xs, (s, e, ntp) = _case(lib, T, k, E, N, K, 56, True)
     kw = dict(epilogue=1, row_flags=lib.A_ROWS_SORTED)

@@ -309,8 +309,7 @@ def moe_gemm(A: torch.Tensor, a_row_div: int, W: PackedWeights, routing: Routing
              dev_err: Optional[torch.Tensor] = None, cta_pairs: int = 0) -> torch.Tensor:
     """The indexed W4A16 GEMM (``w4a16_moe_gemm``).  ``split_k``, ``num_ctas`` and
     ``cta_pairs`` override the planner for measurements (0 = planner; cta_pairs 1 = one CTA per
-    128-row tile, 2 = one M = 256 MMA over two CTAs, 3 = two-CTA clusters sharing the
-    activation tiles by multicast TMA)."""
+    128-row tile, 2 = one M = 256 MMA over two CTAs)."""
     _cuda(A, torch.bfloat16, "A")
     width = W.N // 2 if epilogue == EPILOGUE_SILU_MUL else W.N
     if out is None:

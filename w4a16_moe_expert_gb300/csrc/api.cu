@@ -337,10 +337,12 @@ static w4a16_status_t prepare_gemm(const GemmCall& c, const DeviceFacts& dev, Ge
   const bool pair_ok = R->block_m == 128 && a.a_sorted && split == 1 && a.n_tiles % 2 == 0 &&
                        grid >= 2 && !c.merge_w;
   const int want_pair = c.sched ? c.sched->cta_pairs : 0;
-  if ((want_pair == 2 || want_pair == 3) && !pair_ok)
+  if (want_pair < 0 || want_pair > 2)
+    return fail(W4A16_INVALID_ARG, "cta_pairs %d: supported values are 0, 1, 2", want_pair);
+  if (want_pair == 2 && !pair_ok)
     return fail(W4A16_INVALID_ARG, "CTA pairs need block_m 128, sorted activation rows, an even "
                                    "tile count and no K split");
-  a.pair = want_pair == 3 ? 2 : (want_pair == 2 || (want_pair == 0 && pair_ok && kPairsByDefault)) ? 1 : 0;
+  a.pair = (want_pair == 2 || (want_pair == 0 && pair_ok && kPairsByDefault)) ? 1 : 0;
   if (a.pair) {
     grid &= ~1;
     fast_divisor(static_cast<uint32_t>(a.n_tiles / 2), &a.nt2_magic, &a.nt2_shift);

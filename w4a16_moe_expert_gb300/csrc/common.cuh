@@ -478,15 +478,6 @@ __device__ __forceinline__ void mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, ui
 }
 // Arrive once on the barrier at `bar`'s offset in both CTAs of the pair when the pair MMAs
 // issued so far complete.
-// One CTA's MMAs, their completion signalled on the barrier at this offset in both CTAs of a
-// two-CTA cluster (both read tiles that one of them loads for the pair by multicast TMA).
-__device__ __forceinline__ void mma_commit_mc2(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"(static_cast<uint16_t>(3))
-      : "memory");
-}
-
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
@@ -593,27 +584,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
-// The same tile written at this shared-memory offset in both CTAs of a two-CTA cluster, each
-// CTA's barrier at `bar`'s offset receiving the bytes that land in its memory.
-__device__ __forceinline__ void tma_load_2d_mc2(uint32_t dst, const void* tmap, int x, int y,
-                                                uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "h"(static_cast<uint16_t>(3))
-      : "memory");
-}
-
-// Four rows (y0..y3) of a one-row-high box at column x, placed one after another.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int x, int y0, int y1,
-                                            int y2, int y3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
       : "memory");
 }
 

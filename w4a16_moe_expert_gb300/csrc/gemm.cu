@@ -333,14 +333,12 @@ __device__ __forceinline__ void arrive_handoff(uint32_t bar, bool leader, int la
   }
 }
 
-template <int NT, int KS, bool FUSED, bool PAIR = false, bool MC = false>
+template <int NT, int KS, bool FUSED, bool PAIR = false>
 __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2) {
   using Cfg = GemmCfg<NT, KS, PAIR>;
-  // CL: two-CTA clusters taking the two tiles of a tile pair of one block.  PAIR: one
-  // cta_group::2 MMA over both CTAs.  MC: each CTA runs its own MMAs; the block's activation
-  // tiles are loaded once for both CTAs (multicast TMA, each CTA issuing half of the K
-  // sub-blocks), and an activation slot is free once both CTAs' MMAs have read it.
-  constexpr bool CL = PAIR || MC;
+  // PAIR: two-CTA clusters taking the two tiles of a tile pair of one block, with one
+  // cta_group::2 MMA over both CTAs.
+  constexpr bool CL = PAIR;
   constexpr int S_W = Cfg::kWStages;
   constexpr int S_B = Cfg::kBStages;
   constexpr int S_A = Cfg::kAStages;
@@ -389,7 +387,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
     }
     for (int s = 0; s < S_B; ++s) {
       mbar_init(smem_u32(&bfull[s]), PAIR ? (leader ? 2 : 1) : ((FUSED || gather) ? kGatherThreads : 1));
-      mbar_init(smem_u32(&bempty[s]), MC ? 2 : 1);  // MC: both CTAs' commits
+      mbar_init(smem_u32(&bempty[s]), 1);
     }
     for (int s = 0; s < S_A; ++s) {
       mbar_init(smem_u32(&afull[s]), PAIR ? 8 : 128);  // pairs: one arrival per warp of both CTAs
@@ -591,18 +589,13 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
           if (!__all_sync(0xffffffffu, wait_bar<PAIR>(smem_u32(&bempty[s]), ph ^ 1, abort_flag, a.dev_err)))
             goto tprod_done;
           const uint32_t bb = smem_u32(&bfull[s]);
-          if (lane == 0) mbar_arrive_expect_tx(bb, nsub * Cfg::kSubB);  // MC: both CTAs' halves
+          if (lane == 0) mbar_arrive_expect_tx(bb, nsub * Cfg::kSubB);
           __syncwarp();
           for (int sb = 0; sb < nsub; ++sb) {
             if (lane != static_cast<int>((it * KS + sb) & 31)) continue;
             const uint32_t dst = smem_u32(b_ring + s * Cfg::kBBytes + sb * Cfg::kSubB);
-            if (MC) {
-              if ((sb & 1) == static_cast<int>(crank))
-                tma_load_2d_mc2(dst, &a.tmap_a, (kb + sb) * kBlockK, static_cast<int>(un.b * a.block_m), bb);
-            } else {
-              tma_load_2d(dst, &a.tmap_a, (kb + sb) * kBlockK,
-                          static_cast<int>(un.b * a.block_m + (PAIR ? crank * (NT / 2) : 0)), bb);
-            }
+            tma_load_2d(dst, &a.tmap_a, (kb + sb) * kBlockK,
+                        static_cast<int>(un.b * a.block_m + (PAIR ? crank * (NT / 2) : 0)), bb);
           }
           __syncwarp();
         }
@@ -662,7 +655,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
           if (rows_gathered) fence_proxy_async_smem();  // cp.async (generic proxy) rows -> tensor core
           tc_fence_after();
           if (prev_sbi >= 0) {
-            if (MC) mma_commit_mc2(smem_u32(&bempty[prev_sbi])); else commit_any<PAIR>(smem_u32(&bempty[prev_sbi]));
+            commit_any<PAIR>(smem_u32(&bempty[prev_sbi]));
             commit_any<PAIR>(smem_u32(&aempty[prev_sa]));
           }
           const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((sbi * Cfg::kBBytes) >> 4);
@@ -692,7 +685,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
           prev_sa = sa;
         }
         if (prev_sbi >= 0) {
-          if (MC) mma_commit_mc2(smem_u32(&bempty[prev_sbi])); else commit_any<PAIR>(smem_u32(&bempty[prev_sbi]));
+          commit_any<PAIR>(smem_u32(&bempty[prev_sbi]));
           commit_any<PAIR>(smem_u32(&aempty[prev_sa]));
         }
         commit_any<PAIR>(smem_u32(&accfull[ab]));
@@ -701,12 +694,6 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
     mma_done:
       commit_any<PAIR>(smem_u32(drain));
       wait_bar_plain<PAIR>(smem_u32(drain), 0);
-      if (MC) {
-        // the peer's commits to this CTA's activation slots must all have landed before
-        // either CTA of the cluster exits: wait for the last release of every slot
-        for (uint32_t j = (it > static_cast<uint32_t>(S_B) ? it - S_B : 0); j < it; ++j)
-          wait_bar_plain<false>(smem_u32(&bempty[j % S_B]), (j / S_B) & 1);
-      }
     }
     __syncwarp();
   } else if (warp >= 4 && warp < 8) {
@@ -968,14 +955,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   gemm_body<NT, KS, false, true>(a, a);
 }
 
-// Multicast pairs (128-token blocks): two-CTA clusters, one 128-row tile each, the block's
-// activation tiles loaded once for both.
-template <int NT, int KS>
-__global__ void __launch_bounds__(kGemmThreads, 1)
-    moe_gemm_mc_kernel(const __grid_constant__ GemmArgs a) {
-  gemm_body<NT, KS, false, false, true>(a, a);
-}
-
 // Fused layer: the gate_up GEMM (a, SiLU-and-mul into sorted rows) and the down GEMM (a2, rows
 // of the first by TMA, top-k merge epilogue) walked as one persistent unit sequence.  Down
 // units wait per block for the gate_up tiles of that block, which earlier units of this grid
@@ -1155,11 +1134,10 @@ cudaError_t launch_layer_fused(GemmArgs& a, GemmArgs& a2, int grid, cudaStream_t
   }
 }
 
-template <bool MC>
 static cudaError_t launch_gemm_pair(GemmArgs& args, int grid, bool pdl, cudaStream_t stream) {
   constexpr int NT = 128, KS = StageK<NT>::value;
-  using Cfg = GemmCfg<NT, KS, !MC>;
-  auto kernel = MC ? moe_gemm_mc_kernel<NT, KS> : moe_gemm_pair_kernel<NT, KS>;
+  using Cfg = GemmCfg<NT, KS, true>;
+  auto kernel = moe_gemm_pair_kernel<NT, KS>;
   static bool configured = false;
   if (!configured) {
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1188,12 +1166,10 @@ cudaError_t launch_gemm(GemmArgs& args, int grid, bool pdl, cudaStream_t stream)
   if (args.pair) {  // block_m 128, sorted rows, even tile count, no K split (checked by the caller)
     if (args.block_m != 128 || !args.a_sorted || args.split_k != 1 || args.n_tiles % 2 || grid < 2)
       return cudaErrorInvalidValue;
-    const bool mc = args.pair == 2;
     cudaError_t err = make_act_tmap(&args.tmap_a, args.A, args.capacity, args.K, args.lda,
-                                    mc ? args.block_m : args.block_m / 2);
+                                    args.block_m / 2);
     if (err != cudaSuccess) return err;
-    return mc ? launch_gemm_pair<true>(args, grid, pdl, stream)
-              : launch_gemm_pair<false>(args, grid, pdl, stream);
+    return launch_gemm_pair(args, grid, pdl, stream);
   }
   const int64_t rows = args.a_sorted
                            ? args.capacity

@@ -51,9 +51,8 @@ struct GemmArgs {
   int32_t* sync;
   int64_t sum_elems;
   uint16_t* final_out;
-  // CTA pairs (block_m 128): units are (block, pair of 128-row tiles); divisor n_tiles / 2.
-  // 1: one cta_group::2 MMA over both CTAs; 2: each CTA its own MMAs, activation tiles
-  // loaded once for both by multicast TMA
+  // CTA pairs (block_m 128): units are (block, pair of 128-row tiles); divisor n_tiles / 2;
+  // one cta_group::2 MMA over both CTAs
   int pair;
   uint32_t nt2_magic, nt2_shift;
 };
