@@ -16,15 +16,20 @@ One step covers every T of the sweep:
 value = weight HBM GB/s over the sweep: sum of the packed weight bytes the two
 projections must read (experts with at least one routed row) divided by the sum
 of the per-call gate_up and down times (medians over the steps).  The roofline
-object describes one launch, the decode-shape gate_up GEMM at T = 64: its
-algorithmic bytes (weights + activations in + outputs) over its per-call time,
-against the measured HBM copy peak, with its DRAM traffic from an ncu capture of
-the same sources; it also carries the sweep aggregate over all ten GEMM launches.
-e2e times the public layer call with pinned host inputs copied in and the output
-copied back inside the timed region.  config also reports per-T layer times in
-three modes (separate kernels, top-k merge in the down epilogue, one GEMM kernel),
-and unless --no-extras the sweep with NVFP4 weights, the grouped contracts and
-both kinds of CTA pairs at 128-token blocks.
+object describes the dominant launch, the gate_up GEMM at the largest T
+(128-token blocks, tensor-bound): its algorithmic flops over its per-call device
+time (back-to-back launches on rows already gathered), against the measured
+BF16 peak, with its DRAM traffic from an ncu capture of the same sources; it
+also carries the down GEMM at that T and the decode-shape gate_up GEMM at T = 64
+(HBM-bound).  Algorithmic bytes count outputs as BF16 rows (T_r * N * 2); the
+extra half of the FP32 per-slot down rows is reported apart.  e2e times the
+public layer call with pinned host inputs copied in and the output copied back
+inside the timed region.  config also reports per-T layer times in three modes
+(separate kernels, top-k merge in the down epilogue, one GEMM kernel), the same
+per-call times for the Kimi-K2 EP8 decode, EP8 prefill and TP8 (uniform and
+Zipf routing) workloads with their layer-call times, and unless --no-extras the
+sweep with NVFP4 weights, the grouped contracts and CTA pairs at 128-token
+blocks.
 
 --impl reference times the CPU oracle (single-threaded C++) on a bounded sample
 of the same workload and reports the same metric.
@@ -52,11 +57,13 @@ WORKLOAD = "qwen3_30b_a3b"
 METRIC = "µs/call and weight HBM GB/s (% roofline) for W4A16 MoE gate_up+down on 1 GB300"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# The roofline object describes one launch: the decode-shape gate_up GEMM at this many tokens.
-ROOFLINE_T = 64
-# Its DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum from an ncu capture
-# of that launch), valid only while the GEMM kernel's sources hash to the recorded value.
-ROOFLINE_TRAFFIC = {"sources_sha256": "1fbe94770e0ba47003fdf8a266766394be73f5593de3ce28eaec54f53f00127b", "bytes": 223309312 + 3544576}
+# The roofline object describes the dominant launch of the sweep: the gate_up GEMM at the
+# largest token count (128-token blocks, tensor-bound).  A second object describes the
+# decode-shape gate_up GEMM at this many tokens (HBM-bound).
+DECODE_ROOFLINE_T = 64
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum from an ncu capture of
+# that launch), valid only while the GEMM kernel's sources hash to the recorded value.
+ROOFLINE_TRAFFIC = {}
 GEMM_SOURCES = ("w4a16_moe_expert_gb300/csrc/gemm.cu", "w4a16_moe_expert_gb300/csrc/gemm.cuh",
                 "w4a16_moe_expert_gb300/csrc/common.cuh")
 
@@ -112,8 +119,10 @@ def accounting(wl, T, topk_ids):
     w_dn = e_act * H * I * 9 // 16
     gu = {"weight_bytes": w_gu, "act_bytes": tok_with_local * H * 2, "out_bytes": T_r * I * 2,
           "flops": 2 * T_r * (2 * I) * H}
-    dn = {"weight_bytes": w_dn, "act_bytes": T_r * I * 2, "out_bytes": T_r * H * 4,
-          "flops": 2 * T_r * H * I}
+    # outputs counted as BF16 rows (T_r * N * 2); this design keeps the per-slot down rows in
+    # FP32, whose extra half is reported apart as design overhead, not algorithmic bytes
+    dn = {"weight_bytes": w_dn, "act_bytes": T_r * I * 2, "out_bytes": T_r * H * 2,
+          "fp32_out_extra_bytes": T_r * H * 2, "flops": 2 * T_r * H * I}
     for d in (gu, dn):
         d["bytes"] = d["weight_bytes"] + d["act_bytes"] + d["out_bytes"]
     return {"T": T, "T_r": T_r, "E_act": e_act, "gate_up": gu, "down": dn}
@@ -175,6 +184,51 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def roofline_object(proj, case, us, peaks, peak_src, bound, kernel):
+    """Roofline of one launch: algorithmic flops (tensor) or bytes (hbm) over its per-call
+    device time, against the measured peak."""
+    d = case["acct"][proj]
+    key = f"{proj}_T{case['T']}"
+    rec = ROOFLINE_TRAFFIC.get(key)
+    traffic = rec["bytes"] if rec and gemm_sources_sha256() == rec["sources_sha256"] else None
+    if bound == "tensor":
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        achieved = d["flops"] / (us * 1e-6) / 1e12
+        unit, src = "TFLOP/s", f"bf16_tflops (burst) of {peak_src}"
+    else:
+        peak = float(peaks["hbm_gbs"])
+        achieved = d["bytes"] / (us * 1e-6) / 1e9
+        unit, src = "GB/s", f"hbm_gbs of {peak_src}"
+    return {"bound": bound, "kernel": kernel, "achieved": round(achieved, 1), "peak": peak,
+            "unit": unit, "frac": round(achieved / peak, 4), "peak_source": src,
+            "traffic": traffic, "launch_us": round(us, 2), "algorithmic_bytes": int(d["bytes"]),
+            "algorithmic_flops": int(d["flops"])}
+
+
+def host_cpu():
+    """Host core count and CPU model (lscpu's model name, else /proc/cpuinfo)."""
+    import platform
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for ln in f:
+                    if ln.lower().startswith("model name"):
+                        model = ln.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return {"nproc": os.cpu_count(), "model": model or "unknown", "machine": platform.machine()}
 
 
 # ---- our arm --------------------------------------------------------------------------------
@@ -262,12 +316,9 @@ def run_ours(args, rank, world, local_rank):
     # that every call reads its weights from HBM (>= 2 x L2 of other weight bytes between reuses).
     l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20))
 
-    def copies_for(touched):
-        return int(min(64, max(2, math.ceil(2 * l2 / max(touched, 1)) + 1)))
-
     for c in cases:
-        c["n_gu"] = copies_for(c["acct"]["gate_up"]["weight_bytes"])
-        c["n_dn"] = copies_for(c["acct"]["down"]["weight_bytes"])
+        c["n_gu"] = copies_for(c["acct"]["gate_up"]["weight_bytes"], l2)
+        c["n_dn"] = copies_for(c["acct"]["down"]["weight_bytes"], l2)
         c["R_gu"], c["R_dn"] = max(20, c["n_gu"]), max(20, c["n_dn"])
     w13s = [w13] + [w13.clone() for _ in range(max(c["n_gu"] for c in cases) - 1)]
     w2s = [w2] + [w2.clone() for _ in range(max(c["n_dn"] for c in cases) - 1)]
@@ -551,29 +602,38 @@ def run_ours(args, rank, world, local_rank):
     achieved = alg_bytes / (gemm_us_max * 1e-6) / 1e9
     e2e_value = whole_job_gbps(w_bytes, world, e2e_us_max)
 
-    # roofline of one launch: the gate_up GEMM at ROOFLINE_T tokens (else the smallest T above
-    # one), algorithmic bytes over its per-call time
-    rc = next((c for c in cases if c["T"] == ROOFLINE_T),
-              min(cases, key=lambda c: abs(c["T"] - ROOFLINE_T)))
-    rt = call_us[cases.index(rc)][0]
-    r_bytes = rc["acct"]["gate_up"]["bytes"]
-    r_achieved = r_bytes / (rt * 1e-6) / 1e9
-    traffic = (ROOFLINE_TRAFFIC["bytes"] if rc["T"] == ROOFLINE_T and
-               gemm_sources_sha256() == ROOFLINE_TRAFFIC["sources_sha256"] else None)
-    roofline = {
-        "bound": "hbm",
-        "kernel": (f"moe_gemm_kernel<{rc['block_m']}, {4 if rc['block_m'] <= 64 else 2}> gate_up "
-                   f"with SiLU-and-mul, T={rc['T']}"),
-        "achieved": round(r_achieved, 1),
-        "peak": hbm,
-        "unit": "GB/s",
-        "frac": round(r_achieved / hbm, 4),
-        "peak_source": f"hbm_gbs of {peak_src}",
-        "traffic": traffic,
-        "algorithmic_bytes": int(r_bytes),
-        "sweep_gemm_achieved": round(achieved, 1),
-        "sweep_gemm_frac": round(achieved / hbm, 4),
-    }
+    # the dominant launch alone: the gate_up GEMM (SiLU-and-mul epilogue) of the largest T, on
+    # rows already gathered into aligned order when its blocks are large (the layer's row gather
+    # is a separate kernel); per-call device time of back-to-back launches, rotating weights
+    big = max(cases, key=lambda c: c["T"])
+    if big["block_m"] >= 64:
+        lib.gather_rows(big["x"], wl.top_k, big["routing"], out=big["xs"])
+        big_gemm = lambda i: lib.moe_gemm(  # noqa: E731
+            big["xs"], 1, w13s[i % big["n_gu"]], big["routing"], epilogue=lib.EPILOGUE_SILU_MUL,
+            row_flags=lib.A_ROWS_SORTED | lib.C_ROWS_SORTED, out=big["h"], workspace=big["ws"],
+            expected_rows_per_expert=rows_hint[big["T"]])
+    else:
+        big_gemm = lambda i: gate_up_call(big, w13s[i % big["n_gu"]])  # noqa: E731
+    big_us = per_call_us(big_gemm, big["R_gu"])
+    roofline = roofline_object(
+        "gate_up", big, big_us, peaks, peak_src, "tensor",
+        f"moe_gemm_kernel<{big['block_m']}, {4 if big['block_m'] <= 64 else 2}> gate_up with "
+        f"SiLU-and-mul, {wl.name} T={big['T']}")
+    dc = next((c for c in cases if c["T"] == DECODE_ROOFLINE_T), None)
+    if dc is not None:
+        roofline["decode_launch"] = roofline_object(
+            "gate_up", dc, call_us[cases.index(dc)][0], peaks, peak_src, "hbm",
+            f"moe_gemm_kernel<{dc['block_m']}, {4 if dc['block_m'] <= 64 else 2}> gate_up with "
+            f"SiLU-and-mul, {wl.name} T={dc['T']}")
+    bt = call_us[cases.index(big)][1]
+    d_tc = big["acct"]["down"]["flops"] / (tflops_peak * 1e12)
+    d_hbm = big["acct"]["down"]["bytes"] / (hbm * 1e9)
+    roofline["down_launch"] = roofline_object(
+        "down", big, bt, peaks, peak_src, "tensor" if d_tc > d_hbm else "hbm",
+        f"moe_gemm_kernel<{big['block_m']}, {4 if big['block_m'] <= 64 else 2}> down, FP32 "
+        f"per-slot rows, {wl.name} T={big['T']}")
+    roofline["sweep_gemm_achieved_GBps"] = round(achieved, 1)
+    roofline["sweep_gemm_hbm_frac"] = round(achieved / hbm, 4)
 
     sweep = []
     for c, u, cu, e, ly, fz, one in zip(cases, stage_us, call_us, e2e_us, layer_us, fused_us, one_us):
@@ -587,7 +647,8 @@ def run_ours(args, rank, world, local_rank):
                "layer_e2e_us": round(e, 2),
                "layer_us": round(ly, 2),
                "layer_fused_topk_us": round(fz, 2),
-               "layer_one_kernel_us": round(one, 2)}
+               "layer_one_kernel_us": round(one, 2),
+               "down_fp32_out_extra_MB": round(a["down"]["fp32_out_extra_bytes"] / 1e6, 1)}
         for name, t_us in (("gate_up", cu[0]), ("down", cu[1])):
             d = a[name]
             roof_us = max(d["bytes"] / (hbm * 1e9), d["flops"] / (tflops_peak * 1e12)) * 1e6
@@ -595,6 +656,14 @@ def run_ours(args, rank, world, local_rank):
             row[f"{name}_TFLOPs"] = round(d["flops"] / (t_us * 1e-6) / 1e12, 2)
             row[f"{name}_roofline_frac"] = round(roof_us / t_us, 3)
         sweep.append(row)
+
+    other = {}
+    if not args.no_other_configs:
+        l2b = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20))
+        for name in OTHER_WORKLOADS:
+            other[name] = time_workload(lib, workloads.WORKLOADS[name], dev, per_call_us, hbm,
+                                        tflops_peak, l2b)
+            torch.cuda.empty_cache()
 
     line = {
         "metric": METRIC,
@@ -625,6 +694,7 @@ def run_ours(args, rank, world, local_rank):
                        "every layer stage"),
             "parallelism": "replicas" if world > 1 else "single GPU",
             "sweep": sweep,
+            "other_configs": other,
             **extras,
         },
         "roofline": roofline,
@@ -638,6 +708,97 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
     return line
+
+
+# ---- the other workloads: per-call projection and layer times ---------------------------------
+
+OTHER_WORKLOADS = ("kimi_k2_ep8_decode", "kimi_k2_ep8_prefill", "kimi_k2_tp8", "kimi_k2_tp8_zipf")
+
+
+def copies_for(touched, l2):
+    """Device copies of a packed weight so that >= 2 x L2 of other weight bytes pass between two
+    reads of one copy."""
+    if touched <= 0:
+        return 2
+    return int(min(64, max(2, math.ceil(2 * l2 / touched) + 1)))
+
+
+def time_workload(lib, wl, dev, per_call_us, hbm, tflops_peak, l2, packed=None):
+    """Per-call gate_up and down times (same method as the main sweep) and the layer call's time,
+    for every token count of one workload."""
+    from w4a16_moe_expert_gb300 import workloads
+    if packed is None:
+        w13_q, w13_s, w2_q, w2_s = workloads.draw_layer_weights(wl)
+        packed = (lib.pack_weights(w13_q.to(dev), w13_s.to(dev), paired=True),
+                  lib.pack_weights(w2_q.to(dev), w2_s.to(dev)))
+        del w13_q, w13_s, w2_q, w2_s
+    w13, w2 = packed
+    cases = []
+    for T in wl.tokens:
+        x, ids, tw = workloads.draw_layer_routing(wl, T)
+        a = accounting(wl, T, ids)
+        cases.append((T, x.to(dev), ids.to(dev), tw.to(dev), a,
+                      copies_for(a["gate_up"]["weight_bytes"], l2), copies_for(a["down"]["weight_bytes"], l2)))
+    n13 = max(c[5] for c in cases)
+    n2 = max(c[6] for c in cases)
+    w13s = [w13] + [w13.clone() for _ in range(n13 - 1)]
+    w2s = [w2] + [w2.clone() for _ in range(n2 - 1)]
+    rows = []
+    for T, x, ids, tw, a, n_gu, n_dn in cases:
+        k = wl.top_k
+        bm = lib.plan_block_m(T, k, wl.E, wl.E_global)
+        hint = max(1, round(T * k / wl.E_global))
+        r = lib.moe_align(ids, wl.E, bm)
+        cap = r.capacity
+        xs = torch.empty((cap, wl.H), dtype=torch.bfloat16, device=dev) if bm >= 64 else None
+        h = torch.empty((cap, wl.I), dtype=torch.bfloat16, device=dev)
+        y = torch.empty((T * k, wl.H), dtype=torch.float32, device=dev)
+        out = torch.empty((T, wl.H), dtype=torch.bfloat16, device=dev)
+        ws = lib.gemm_workspace(T * k, wl.E, 2 * wl.I, wl.H, bm, dev)
+        lws = torch.empty(lib.layer_workspace_size(T, k, wl.E, wl.H, wl.I, wl.E_global, bm),
+                          dtype=torch.uint8, device=dev)
+
+        def gate_up(i):
+            W = w13s[i % n_gu]
+            if bm >= 64:
+                lib.gather_rows(x, k, r, out=xs)
+                lib.moe_gemm(xs, 1, W, r, epilogue=lib.EPILOGUE_SILU_MUL,
+                             row_flags=lib.A_ROWS_SORTED | lib.C_ROWS_SORTED, out=h, workspace=ws,
+                             expected_rows_per_expert=hint)
+            else:
+                lib.moe_gemm(x, k, W, r, epilogue=lib.EPILOGUE_SILU_MUL,
+                             row_flags=lib.C_ROWS_SORTED, out=h, workspace=ws,
+                             expected_rows_per_expert=hint)
+
+        def down(i):
+            lib.moe_gemm(h, 1, w2s[i % n_dn], r, row_flags=lib.A_ROWS_SORTED | lib.C_FP32, out=y,
+                         workspace=ws, expected_rows_per_expert=hint)
+
+        def layer(i):
+            lib.moe_layer(x, w13s[i % n_gu], w2s[i % n_dn], ids, tw, E_global=wl.E_global,
+                          block_m=bm, out=out, workspace=lws)
+
+        gu = per_call_us(gate_up, max(20, n_gu))
+        dn = per_call_us(down, max(20, n_dn))
+        ly = per_call_us(layer, max(20, n_gu, n_dn))
+        row = {"T": T, "T_r": a["T_r"], "E_act": a["E_act"], "block_m": bm,
+               "gate_up_us": round(gu, 2), "down_us": round(dn, 2),
+               "gate_up_plus_down_us": round(gu + dn, 2), "layer_us": round(ly, 2)}
+        for name, t_us in (("gate_up", gu), ("down", dn)):
+            d = a[name]
+            t_hbm = d["bytes"] / (hbm * 1e9) * 1e6
+            t_tc = d["flops"] / (tflops_peak * 1e12) * 1e6
+            row[f"{name}_weight_GBps"] = round(d["weight_bytes"] / (t_us * 1e-6) / 1e9, 1)
+            row[f"{name}_TFLOPs"] = round(d["flops"] / (t_us * 1e-6) / 1e12, 2)
+            row[f"{name}_bound"] = "tensor" if t_tc > t_hbm else "hbm"
+            row[f"{name}_roofline_frac"] = round(max(t_hbm, t_tc) / t_us, 3) if a["T_r"] else None
+        rows.append(row)
+        del xs, h, y, out, ws, lws
+    del w13s, w2s
+    return {"workload": (f"{wl.name}: {wl.E} local of {wl.E_global} experts, top-{wl.top_k}, "
+                         f"hidden {wl.H}, gate_up [{wl.E},{2 * wl.I},{wl.H}], down "
+                         f"[{wl.E},{wl.H},{wl.I}], {wl.routing} routing"),
+            "sweep": rows}
 
 
 # ---- CPU oracle (baseline and reference arm) --------------------------------------------------
@@ -666,8 +827,10 @@ def oracle_sample(wl, budget_s):
 def cpu_baseline(wl, budget_s=15.0):
     b, s, Ts = oracle_sample(wl, budget_s)
     return {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"single-threaded C++ oracle, whole layer at T in {Ts} "
-                      f"({s:.1f} s of CPU work; weight bytes of those calls / time)"}
+            "host": host_cpu(), "extrapolated": False,
+            "sample": f"single-threaded C++ oracle on 1 of the host's cores, whole layer at T in "
+                      f"{Ts} of the sweep, measured, not extrapolated ({s:.1f} s of CPU work; "
+                      f"weight bytes of those calls / time)"}
 
 
 def run_reference(args, rank, world, local_rank):
@@ -682,8 +845,9 @@ def run_reference(args, rank, world, local_rank):
             bytes_ = b
     mean_s = statistics.fmean(times)
     value = bytes_ / mean_s / 1e9
-    sample = (f"single-threaded C++ oracle, whole layer at T in {Ts} per step "
-              f"(the oracle as written; weight bytes / time)")
+    sample = (f"single-threaded C++ oracle on 1 of the host's cores, whole layer at T in {Ts} "
+              f"per step (the oracle as written; weight bytes / time; measured, not "
+              f"extrapolated)")
     return {
         "impl": "reference",
         "metric": METRIC,
@@ -702,7 +866,7 @@ def run_reference(args, rank, world, local_rank):
                                f"gate_up [{wl.E},{2 * wl.I},{wl.H}], down [{wl.E},{wl.H},{wl.I}], "
                                f"uint4 group-32 BF16 scales", "tokens": Ts},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "host": host_cpu(), "extrapolated": False, "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -721,7 +885,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of a graph")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the NVFP4 and grouped-contract measurements")
+                    help="skip the NVFP4, grouped-contract and CTA-pair measurements")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip the Kimi-K2 EP8 decode / EP8 prefill / TP8 sweeps")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps are required")

@@ -262,7 +262,9 @@ w4a16_status_t w4a16_masked_gemm(const uint16_t* A, int64_t lda, int G, int max_
  * (arrival counters and FP32 partial sums) is a library-owned device array of
  * W4A16_STATIC_SCRATCH_BYTES that every GPU loading the library keeps until the process
  * exits.  The first call on a device looks up that array's device address (once per device,
- * with the device current); make that first call before any stream capture.  Each call
+ * with the device current); make that first call before any stream capture.  The address
+ * belongs to the device's CUDA context: after a device reset the next call looks it up again
+ * in the new context (so make that call before any capture too).  Each call
  * clears the counter words it needs with an asynchronous memset on `stream` and calls no
  * cudaMalloc, cudaFree or other allocating routine.  All calls share the one array: calls
  * whose kernels may overlap on the GPU (different streams, or concurrent host threads) race
@@ -319,6 +321,13 @@ w4a16_status_t w4a16_topk_sum(const float* Y, const int32_t* topk_ids,
  * Kernels: align, (row gather for block_m >= 64), the fused GEMM.  Not bitwise reproducible,
  * as for W4A16_LAYER_FUSED_TOPK; implies it. */
 #define W4A16_LAYER_FUSED 0x2u
+/* Test hook for the bounded-wait error path, with W4A16_LAYER_FUSED only: every down unit
+ * waits for one more finished gate_up tile than its block has, with a limit of 2^20 cycles
+ * (about half a millisecond) instead of about a second.  Every such wait runs out: the CTA
+ * gives up its remaining units, drains its copies, frees its tensor memory and returns, and
+ * W4A16_DEVERR_TIMEOUT is set in *dev_err.  The call itself returns W4A16_OK; out is
+ * incomplete.  Not for production use. */
+#define W4A16_LAYER_DEBUG_WAIT_TIMEOUT 0x80000000u
 int w4a16_plan_block_m(int T, int top_k, int E, int E_global);
 size_t w4a16_layer_workspace_size(int T, int top_k, int E, int E_global, int H, int I,
                                   int block_m);

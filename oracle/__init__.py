@@ -57,7 +57,7 @@ def lib():
                 "w4a16_oracle_align_capacity": (i64, [i32, i32, i32, i32]),
                 "w4a16_oracle_align": (i32, [vp, i32, i32, i32, i32, i64, vp, vp, vp]),
                 "w4a16_oracle_dequant": (None, [vp, vp, i64, i32, i32, vp]),
-                "w4a16_oracle_gemm_rows": (None, [vp, i32, i32, vp, vp, i32, i32, vp, vp, i64, vp]),
+                "w4a16_oracle_gemm_rows": (None, [vp, i32, i32, vp, vp, i32, i32, vp, vp, i64, vp, vp]),
                 "w4a16_oracle_moe_gemm": (i32, [vp, i32, i32, vp, vp, i32, i32, vp, vp, i32, i32,
                                                 i32, i32, i32, vp, vp]),
                 "w4a16_oracle_contiguous_gemm": (i32, [vp, i64, i32, vp, vp, i32, i32, i32, vp, vp]),
@@ -147,8 +147,15 @@ def dequant(qweight, scales, group: int = 32) -> torch.Tensor:
     return _bf16_tensor(out)
 
 
-def gemm_rows(A, a_row_div: int, qweight, scales, slots, experts, group: int = 32) -> torch.Tensor:
-    """out[r] = A[slots[r] // a_row_div] @ dequant(W[experts[r]]).T, bf16 [len(slots), N]."""
+def gemm_rows(A, a_row_div: int, qweight, scales, slots, experts, group: int = 32,
+              out_f32: bool = False, threads: int = 1) -> torch.Tensor:
+    """out[r] = A[slots[r] // a_row_div] @ dequant(W[experts[r]]).T: bf16 [len(slots), N], or the
+    unrounded FP32 sums with ``out_f32``.
+
+    With ``threads > 1`` the same single-threaded function runs over disjoint row ranges on
+    that many host threads; every output element has the same arithmetic, so the result is
+    identical.
+    """
     a = _np(A, np.uint16)
     q = _np(qweight, np.int32)
     s = _np(scales, np.uint16)
@@ -156,10 +163,25 @@ def gemm_rows(A, a_row_div: int, qweight, scales, slots, experts, group: int = 3
     ex = _np(np.asarray(experts), np.int32)
     K = a.shape[-1]
     N = q.shape[-2]
-    out = np.empty((sl.size, N), np.uint16)
-    lib().w4a16_oracle_gemm_rows(_ptr(a), a_row_div, K, _ptr(q), _ptr(s), N, group, _ptr(sl),
-                                 _ptr(ex), sl.size, _ptr(out))
-    return _bf16_tensor(out)
+    out = np.empty((sl.size, N), np.float32 if out_f32 else np.uint16)
+    L = lib()
+
+    def run(lo, hi):
+        if hi <= lo:
+            return
+        L.w4a16_oracle_gemm_rows(_ptr(a), a_row_div, K, _ptr(q), _ptr(s), N, group,
+                                 _ptr(sl[lo:hi]), _ptr(ex[lo:hi]), hi - lo,
+                                 None if out_f32 else _ptr(out[lo:hi]),
+                                 _ptr(out[lo:hi]) if out_f32 else None)
+
+    threads = max(1, min(threads, sl.size))
+    if threads == 1:
+        run(0, sl.size)
+    else:
+        cuts = np.linspace(0, sl.size, threads + 1).astype(np.int64)
+        with ThreadPoolExecutor(threads) as pool:
+            list(pool.map(lambda lh: run(int(lh[0]), int(lh[1])), zip(cuts[:-1], cuts[1:])))
+    return torch.from_numpy(out) if out_f32 else _bf16_tensor(out)
 
 
 def moe_gemm(A, a_row_div: int, qweight, scales, sorted_ids, expert_ids, ntp: int, block_m: int,

@@ -241,13 +241,16 @@ void w4a16_oracle_dequant(const int32_t* qweight, const uint16_t* scales, int64_
 
 // ---- gemm ----------------------------------------------------------------------
 
-// out[r, :] = A[slots[r] / a_row_div] . dequant(W[experts[r]])^T for r < nrows.
+// out[r, :] = A[slots[r] / a_row_div] . dequant(W[experts[r]])^T for r < nrows: BF16 rows in
+// out, or the unrounded FP32 sums in out_f32 when it is not NULL.
 void w4a16_oracle_gemm_rows(const uint16_t* A, int a_row_div, int K, const int32_t* qweight,
                             const uint16_t* scales, int N, int group, const int32_t* slots,
-                            const int32_t* experts, int64_t nrows, uint16_t* out) {
+                            const int32_t* experts, int64_t nrows, uint16_t* out,
+                            float* out_f32) {
   for (int64_t r = 0; r < nrows; ++r) {
     const uint16_t* a = A + static_cast<int64_t>(slots[r] / a_row_div) * K;
-    gemm_one_row(a, K, qweight, scales, N, group, experts[r], out + r * N);
+    gemm_one_row(a, K, qweight, scales, N, group, experts[r], out_f32 ? nullptr : out + r * N,
+                 out_f32 ? out_f32 + r * N : nullptr);
   }
 }
 

@@ -329,6 +329,30 @@ def test_gemm_rows_matches_indexed_gemm():
     assert torch.equal(bits_t(rows), bits_t(C))
 
 
+def test_gemm_rows_fp32_within_the_sequential_summation_bound():
+    # FP32 rows against an exact float64 dot of the same BF16 operands: a left-to-right FP32
+    # sum of K exactly representable products is within (K - 1) * 2^-24 * sum|p| of the truth;
+    # rounded to BF16 they are the BF16 rows bit for bit; host threads change nothing
+    qw, sc, x, ids, _ = _tiny_problem(23, T=12, E=4)
+    T, k = ids.shape
+    slots = np.arange(T * k)
+    experts = ids.reshape(-1).numpy()
+    r32 = oracle.gemm_rows(x, k, qw, sc, slots, experts, out_f32=True)
+    r16 = oracle.gemm_rows(x, k, qw, sc, slots, experts)
+    assert r32.dtype == torch.float32
+    assert torch.equal(bits_t(r32.to(torch.bfloat16)), bits_t(r16))
+    wd = dequant_np(qw.numpy(), sc.view(torch.int16).numpy())
+    xa = bf16_np(x)
+    K = xa.shape[1]
+    for i in range(T * k):
+        prods = wd[experts[i]] * xa[i // k][None, :]
+        exact = prods.sum(axis=1)
+        bound = (K - 1) * 2.0 ** -24 * np.abs(prods).sum(axis=1)
+        assert np.all(np.abs(r32[i].numpy().astype(np.float64) - exact) <= bound + 1e-30)
+    r32t = oracle.gemm_rows(x, k, qw, sc, slots, experts, out_f32=True, threads=5)
+    assert torch.equal(r32t, r32)
+
+
 def test_gemm_fp32_output_rounds_to_the_bf16_output():
     qw, sc, x, ids, _ = _tiny_problem(19)
     T, k = ids.shape

@@ -37,6 +37,7 @@ PACK_GATE_UP_PAIRED = 0x1
 PACK_NVFP4 = 0x2
 LAYER_FUSED_TOPK = 0x1
 LAYER_FUSED = 0x2
+LAYER_DEBUG_WAIT_TIMEOUT = 0x80000000  # test hook: the fused layer's cross-CTA waits run out
 PACK_MAGIC = 0x3631413457454F4D
 PACK_VERSION = 2
 
@@ -443,10 +444,12 @@ def moe_layer(x: torch.Tensor, w13: PackedWeights, w2: PackedWeights, topk_ids: 
               topk_weights: torch.Tensor, E_global: int = 0, block_m: int = 0,
               out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
               dev_err: Optional[torch.Tensor] = None, fused_topk: bool = False,
-              fused: bool = False) -> torch.Tensor:
+              fused: bool = False, debug_wait_timeout: bool = False) -> torch.Tensor:
     """The whole layer; ``fused_topk`` merges the top-k outputs inside the down GEMM
     (atomic FP32 sums: within the tolerance, not bitwise reproducible); ``fused`` also runs
-    gate_up and down as one persistent kernel (and implies ``fused_topk``)."""
+    gate_up and down as one persistent kernel (and implies ``fused_topk``).
+    ``debug_wait_timeout`` (with ``fused``; tests only) makes every cross-CTA wait of the down
+    units run out after a short limit (``W4A16_LAYER_DEBUG_WAIT_TIMEOUT``)."""
     _cuda(x, torch.bfloat16, "x")
     _cuda(topk_ids, torch.int32, "topk_ids")
     _cuda(topk_weights, torch.float32, "topk_weights")
@@ -459,7 +462,8 @@ def moe_layer(x: torch.Tensor, w13: PackedWeights, w2: PackedWeights, topk_ids: 
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
     _check("w4a16_moe_layer_ex", load().w4a16_moe_layer_ex(
         _ptr(x), ctypes.byref(w13.desc), ctypes.byref(w2.desc), _ptr(topk_ids), _ptr(topk_weights),
-        T, k, E_global, block_m, (LAYER_FUSED if fused else 0) | (LAYER_FUSED_TOPK if fused_topk else 0),
+        T, k, E_global, block_m, (LAYER_FUSED if fused else 0) | (LAYER_FUSED_TOPK if fused_topk else 0)
+        | (LAYER_DEBUG_WAIT_TIMEOUT if debug_wait_timeout else 0),
         _ptr(out), _ptr(workspace),
         workspace.numel(), _ptr(dev_err), _stream()))
     return out

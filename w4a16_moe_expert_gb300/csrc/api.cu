@@ -747,9 +747,11 @@ w4a16_status_t w4a16_moe_layer_ex(const uint16_t* x, const w4a16_packed_weights_
                                   int block_m, uint32_t layer_flags, uint16_t* out,
                                   void* workspace, size_t workspace_bytes, int32_t* dev_err,
                                   w4a16_stream_t stream) {
-  if (layer_flags & ~(W4A16_LAYER_FUSED_TOPK | W4A16_LAYER_FUSED))
+  if (layer_flags & ~(W4A16_LAYER_FUSED_TOPK | W4A16_LAYER_FUSED | W4A16_LAYER_DEBUG_WAIT_TIMEOUT))
     return fail(W4A16_INVALID_ARG, "unknown layer flags");
   const bool one_kernel = (layer_flags & W4A16_LAYER_FUSED) != 0;
+  if ((layer_flags & W4A16_LAYER_DEBUG_WAIT_TIMEOUT) && !one_kernel)
+    return fail(W4A16_INVALID_ARG, "W4A16_LAYER_DEBUG_WAIT_TIMEOUT needs W4A16_LAYER_FUSED");
   const bool fused = one_kernel || (layer_flags & W4A16_LAYER_FUSED_TOPK) != 0;
   w4a16_status_t st = check_packed(w13);
   if (st != W4A16_OK) return st;
@@ -834,6 +836,10 @@ w4a16_status_t w4a16_moe_layer_ex(const uint16_t* x, const w4a16_packed_weights_
     a1.signal_done = blk_done;
     a2.wait_done = blk_done;
     a2.wait_count = a1.n_tiles;
+    if (layer_flags & W4A16_LAYER_DEBUG_WAIT_TIMEOUT) {  // a count nothing reaches, short limit
+      a2.wait_count = a1.n_tiles + 1;
+      a2.wait_limit = 1ll << 20;
+    }
     a2.routing_ready = a1.routing_ready;
     // the kernel zeroes the sums, merges into them and rounds them into out
     a2.sync = blk_done + L.cap / L.block_m;

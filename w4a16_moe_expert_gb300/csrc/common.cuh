@@ -324,14 +324,15 @@ __device__ __forceinline__ void red_release_add(int32_t* p, int32_t v) {
 // before the increments is visible afterwards).  On timeout the CTA's abort flag and the
 // caller's error word are set.
 __device__ __forceinline__ bool wait_count_at_least(const int32_t* p, int32_t want,
-                                                    volatile int* abort_flag, int32_t* dev_err) {
+                                                    volatile int* abort_flag, int32_t* dev_err,
+                                                    long long limit = kWaitLimitCycles) {
   const long long t0 = clock64();
   while (true) {
     int32_t v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     if (v >= want) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       set_dev_err(dev_err, W4A16_DEVERR_TIMEOUT);
       *abort_flag = 1;
       return false;

@@ -486,7 +486,9 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
         if (!un.ok) continue;
         const GemmArgs& g = args_of<FUSED>(a, a2, un);
         if (g.wait_done) {
-          if (gt == 0) wait_count_at_least(g.wait_done + un.b, g.wait_count, abort_flag, g.dev_err);
+          if (gt == 0)
+            wait_count_at_least(g.wait_done + un.b, g.wait_count, abort_flag, g.dev_err,
+                                g.wait_limit > 0 ? g.wait_limit : kWaitLimitCycles);
           named_bar_act();
           if (*abort_flag) goto fprod_done;
           fence_proxy_async_global();

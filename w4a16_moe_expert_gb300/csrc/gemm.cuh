@@ -45,6 +45,7 @@ struct GemmArgs {
   int32_t* signal_done;
   const int32_t* wait_done;
   int wait_count;
+  long long wait_limit;  // cycles before that wait gives up (0: the default, about a second)
   // single-kernel layer, down GEMM only: sync[0] counts CTAs that zeroed their slice of the
   // FP32 token sums C (sum_elems floats), sync[1] CTAs whose units are all done; the last
   // phase rounds the sums into final_out (BF16)

@@ -22,22 +22,48 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 
 namespace {
 std::mutex g_scratch_mu;
-void* g_scratch_ptr[64] = {};  // device address of g_static_scratch, per device ordinal
+// Device address of g_static_scratch per device ordinal, with the CUDA context it was looked
+// up in: a device reset (or a released and re-created primary context) gives the device a new
+// context, in which the array has a new address, so the lookup is repeated then.
+void* g_scratch_ptr[64] = {};
+void* g_scratch_ctx[64] = {};
+
+typedef int (*CtxGetCurrentFn)(void**);  // cuCtxGetCurrent, fetched from the driver at run time
+
+void* current_context() {
+  static CtxGetCurrentFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    tried = true;
+  }
+  void* ctx = nullptr;
+  if (fn && fn(&ctx) != 0) ctx = nullptr;
+  return ctx;
+}
 }  // namespace
 
-// Device address of the array for the current device, looked up once per device.  (In host
-// code the array's name is only a host-side stand-in, not a device address.)
+// Device address of the array for the current device, looked up on the first call in each
+// device's context.  (In host code the array's name is only a host-side stand-in, not a device
+// address.)
 static cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const void* ctx = current_context();  // NULL before the runtime has set up the device
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  if (!g_scratch_ptr[dev] || !ctx || g_scratch_ctx[dev] != ctx) {
     void* p = nullptr;
-    err = cudaGetSymbolAddress(&p, g_static_scratch);
+    err = cudaGetSymbolAddress(&p, g_static_scratch);  // sets up the device's context if needed
     if (err != cudaSuccess) return err;
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = current_context();
   }
   *out = g_scratch_ptr[dev];
   return cudaSuccess;
