@@ -60,8 +60,9 @@ def lib():
                 "w4a16_oracle_gemm_rows": (None, [vp, i32, i32, vp, vp, i32, i32, vp, vp, i64, vp, vp]),
                 "w4a16_oracle_moe_gemm": (i32, [vp, i32, i32, vp, vp, i32, i32, vp, vp, i32, i32,
                                                 i32, i32, i32, vp, vp]),
-                "w4a16_oracle_contiguous_gemm": (i32, [vp, i64, i32, vp, vp, i32, i32, i32, vp, vp]),
-                "w4a16_oracle_masked_gemm": (i32, [vp, i32, i32, i32, vp, vp, i32, i32, vp, vp]),
+                "w4a16_oracle_contiguous_gemm": (i32, [vp, i64, i32, vp, vp, i32, i32, i32, vp, vp,
+                                                       vp]),
+                "w4a16_oracle_masked_gemm": (i32, [vp, i32, i32, i32, vp, vp, i32, i32, vp, vp, vp]),
                 "w4a16_oracle_nvfp4_dequant": (None, [vp, vp, i64, i32, vp]),
                 "w4a16_oracle_nvfp4_moe_gemm": (i32, [vp, i32, i32, vp, vp, i32, vp, vp, i32, i32,
                                                       i32, i32, i32, vp, vp]),
@@ -266,25 +267,30 @@ def nvfp4_moe_gemm(A, a_row_div: int, codes, scales, sorted_ids, expert_ids, ntp
     return torch.from_numpy(C) if out_f32 else _bf16_tensor(C)
 
 
-def contiguous_gemm(A, qweight, scales, m_indices, group: int = 32) -> torch.Tensor:
-    """Contiguous grouped layout: C[r] = A[r] @ dequant(W[m_indices[r]]).T, padding rows 0."""
+def contiguous_gemm(A, qweight, scales, m_indices, group: int = 32,
+                    out_f32: bool = False) -> torch.Tensor:
+    """Contiguous grouped layout: C[r] = A[r] @ dequant(W[m_indices[r]]).T, padding rows 0;
+    BF16, or the unrounded FP32 sums with ``out_f32``."""
     a = _np(A, np.uint16)
     q = _np(qweight, np.int32)
     s = _np(scales, np.uint16)
     mi = _np(m_indices, np.int32)
     m, K = a.shape
     E, N = q.shape[0], q.shape[1]
-    C = np.zeros((m, N), np.uint16)
+    C = np.zeros((m, N), np.float32 if out_f32 else np.uint16)
     rc = lib().w4a16_oracle_contiguous_gemm(_ptr(a), m, K, _ptr(q), _ptr(s), E, N, group,
-                                            _ptr(mi), _ptr(C))
+                                            _ptr(mi), None if out_f32 else _ptr(C),
+                                            _ptr(C) if out_f32 else None)
     if rc:
         raise ValueError(f"oracle contiguous_gemm failed with code {rc}")
-    return _bf16_tensor(C)
+    return torch.from_numpy(C) if out_f32 else _bf16_tensor(C)
 
 
-def masked_gemm(A, qweight, scales, masked_m, max_m: int, group: int = 32) -> torch.Tensor:
+def masked_gemm(A, qweight, scales, masked_m, max_m: int, group: int = 32,
+                out_f32: bool = False) -> torch.Tensor:
     """Masked grouped layout over A [G * max_m, K]: rows g*max_m + r, r < masked_m[g], of the
-    flat [G * max_m, N] output; the other rows are returned as 0 (undefined by the contract)."""
+    flat [G * max_m, N] output; the other rows are returned as 0 (undefined by the contract).
+    BF16, or the unrounded FP32 sums with ``out_f32``."""
     a = _np(A, np.uint16).reshape(-1, _np(A, np.uint16).shape[-1])
     q = _np(qweight, np.int32)
     s = _np(scales, np.uint16)
@@ -292,16 +298,22 @@ def masked_gemm(A, qweight, scales, masked_m, max_m: int, group: int = 32) -> to
     G = q.shape[0]
     N = q.shape[1]
     K = a.shape[-1]
-    C = np.zeros((G * max_m, N), np.uint16)
+    C = np.zeros((G * max_m, N), np.float32 if out_f32 else np.uint16)
     rc = lib().w4a16_oracle_masked_gemm(_ptr(a), G, max_m, K, _ptr(q), _ptr(s), N, group,
-                                        _ptr(mm), _ptr(C))
+                                        _ptr(mm), None if out_f32 else _ptr(C),
+                                        _ptr(C) if out_f32 else None)
     if rc:
         raise ValueError(f"oracle masked_gemm failed with code {rc}")
-    return _bf16_tensor(C)
+    return torch.from_numpy(C) if out_f32 else _bf16_tensor(C)
 
 
 def silu_mul(C) -> torch.Tensor:
-    c = _np(C, np.uint16)
+    """C [rows, 2I] gate_up sums -> h bf16 [rows, I], h = bf16(silu(gate) * up).  The sums are
+    meant unrounded (FP32, e.g. ``gemm_rows(..., out_f32=True)``); BF16 input is widened
+    exactly."""
+    if isinstance(C, torch.Tensor):
+        C = C.detach().cpu().float()
+    c = _np(C, np.float32)
     rows, two_i = c.shape
     h = np.empty((rows, two_i // 2), np.uint16)
     lib().w4a16_oracle_silu_mul(_ptr(c), rows, two_i // 2, _ptr(h))
@@ -349,7 +361,8 @@ def moe_layer_parallel(x, w13_q, w13_s, w2_q, w2_s, topk_ids, topk_weights, bloc
     T, k = ids.shape
     E = int(_np(w13_q, np.int32).shape[0])
     sorted_ids, expert_ids, ntp = moe_align(ids, E, block_m)
-    c13 = moe_gemm(x, k, w13_q, w13_s, sorted_ids, expert_ids, ntp, block_m, T * k, threads=threads)
+    c13 = moe_gemm(x, k, w13_q, w13_s, sorted_ids, expert_ids, ntp, block_m, T * k, threads=threads,
+                   out_f32=True)
     h = silu_mul(c13)
     y = moe_gemm(h, 1, w2_q, w2_s, sorted_ids, expert_ids, ntp, block_m, T * k, threads=threads,
                  out_f32=True)

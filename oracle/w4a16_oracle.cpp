@@ -28,14 +28,18 @@
 //    C[i, :] = A[i / a_row_div] . dequant(W[expert_ids[p / block_m]])^T,
 //    a plain FP32 dot product over k ascending, rounded once to BF16.
 //  * silu_mul -- SiLU(gate) * up with gate = C[:, :I], up = C[:, I:], on the
-//    BF16 gate_up output; evaluated in double, rounded once to BF16.
+//    unrounded FP32 gate_up sums (the SiLU-and-mul is fused between the two
+//    GEMMs, so no BF16 gate_up tensor exists on the path; rounding gate and
+//    up to BF16 first and then h again stacks two order-dependent roundings,
+//    up to 1.5% of |h| at the top of a binade, beyond the stated output
+//    tolerance); evaluated in double, rounded once to BF16.
 //  * topk_sum -- out[t, :] = sum over valid slots s (ascending) of
 //    topk_weights[t, s] * Y[t*top_k + s, :]; double, rounded once to BF16.
 //    The per-slot down outputs Y stay FP32 (the pages fix no precision for
 //    them; rounding them to BF16 first would add up to half a BF16 ulp of the
 //    largest per-slot value, an error as large as the stated output
 //    tolerance, so the reading that fits that tolerance keeps them in FP32).
-//  * layer -- align, gate_up gemm (BF16 out), silu_mul, down gemm (FP32 out),
+//  * layer -- align, gate_up gemm (FP32 out), silu_mul, down gemm (FP32 out),
 //    topk_sum in that
 //    order (Chord page, "Measurements": the per-layer time is gate_up plus
 //    down; "humans& ..." page: FC1, FC2 and the top-K merge).
@@ -277,12 +281,13 @@ int w4a16_oracle_moe_gemm(const uint16_t* A, int a_row_div, int K, const int32_t
 
 // ---- activation and combine -----------------------------------------------------
 
-// C bf16 [rows, 2I] -> h bf16 [rows, I]: h = bf16(silu(gate) * up).
-void w4a16_oracle_silu_mul(const uint16_t* C, int64_t rows, int I, uint16_t* h) {
+// C fp32 [rows, 2I] (the unrounded gate_up sums) -> h bf16 [rows, I]:
+// h = bf16(silu(gate) * up).
+void w4a16_oracle_silu_mul(const float* C, int64_t rows, int I, uint16_t* h) {
   for (int64_t r = 0; r < rows; ++r) {
     for (int j = 0; j < I; ++j) {
-      const double g = bf16_to_float(C[r * 2 * I + j]);
-      const double u = bf16_to_float(C[r * 2 * I + I + j]);
+      const double g = C[r * 2 * I + j];
+      const double u = C[r * 2 * I + I + j];
       const double silu = g / (1.0 + std::exp(-g));
       h[r * I + j] = double_to_bf16(silu * u);
     }
@@ -339,18 +344,23 @@ int w4a16_oracle_nvfp4_moe_gemm(const uint16_t* A, int a_row_div, int K, const u
 // concatenated by expert, each group padded to a 128-row boundary, with m_indices[r] the
 // expert of row r or -1 for padding; the output row r is A[r] times the dequantised weight of
 // that expert.  Padding rows are zero here.
+// C is BF16, or FP32 (the unrounded sums) when C_f32 is not NULL.
 int w4a16_oracle_contiguous_gemm(const uint16_t* A, int64_t m, int K, const int32_t* qweight,
                                  const uint16_t* scales, int E, int N, int group,
-                                 const int32_t* m_indices, uint16_t* C) {
+                                 const int32_t* m_indices, uint16_t* C, float* C_f32) {
   if (K % 8 || K % group || m % 128) return -3;
   for (int64_t r = 0; r < m; ++r) {
     const int32_t e = m_indices[r];
-    uint16_t* out = C + r * N;
+    uint16_t* out = C_f32 ? nullptr : C + r * N;
+    float* out_f32 = C_f32 ? C_f32 + r * N : nullptr;
     if (e < 0 || e >= E) {
-      for (int n = 0; n < N; ++n) out[n] = 0;
+      for (int n = 0; n < N; ++n) {
+        if (out) out[n] = 0;
+        if (out_f32) out_f32[n] = 0.0f;
+      }
       continue;
     }
-    gemm_one_row(A + r * K, K, qweight, scales, N, group, e, out, nullptr);
+    gemm_one_row(A + r * K, K, qweight, scales, N, group, e, out, out_f32);
   }
   return 0;
 }
@@ -360,13 +370,14 @@ int w4a16_oracle_contiguous_gemm(const uint16_t* A, int64_t m, int K, const int3
 // masked_m[g] are valid; only those output rows are defined (the others are left as they are).
 int w4a16_oracle_masked_gemm(const uint16_t* A, int G, int max_m, int K, const int32_t* qweight,
                              const uint16_t* scales, int N, int group, const int32_t* masked_m,
-                             uint16_t* C) {
+                             uint16_t* C, float* C_f32) {
   if (K % 8 || K % group || max_m <= 0) return -3;
   for (int g = 0; g < G; ++g) {
     const int valid = masked_m[g] < 0 ? 0 : (masked_m[g] > max_m ? max_m : masked_m[g]);
     for (int r = 0; r < valid; ++r) {
       const int64_t row = static_cast<int64_t>(g) * max_m + r;
-      gemm_one_row(A + row * K, K, qweight, scales, N, group, g, C + row * N, nullptr);
+      gemm_one_row(A + row * K, K, qweight, scales, N, group, g, C_f32 ? nullptr : C + row * N,
+                   C_f32 ? C_f32 + row * N : nullptr);
     }
   }
   return 0;
@@ -385,11 +396,11 @@ int w4a16_oracle_moe_layer(const uint16_t* x, const int32_t* w13_q, const uint16
   int rc = w4a16_oracle_align(topk_ids, T, top_k, E, block_m, cap, sorted_ids.data(),
                               expert_ids.data(), &ntp);
   if (rc) return rc;
-  std::vector<uint16_t> c13(slots * 2 * I, 0), h(slots * I, 0);
-  std::vector<float> y(slots * H, 0.0f);
+  std::vector<float> c13(slots * 2 * I, 0.0f), y(slots * H, 0.0f);
+  std::vector<uint16_t> h(slots * I, 0);
   rc = w4a16_oracle_moe_gemm(x, top_k, H, w13_q, w13_s, 2 * I, group, sorted_ids.data(),
                              expert_ids.data(), ntp, block_m, static_cast<int>(slots), 0, E,
-                             c13.data(), nullptr);
+                             nullptr, c13.data());
   if (rc) return rc;
   w4a16_oracle_silu_mul(c13.data(), slots, I, h.data());
   rc = w4a16_oracle_moe_gemm(h.data(), 1, I, w2_q, w2_s, H, group, sorted_ids.data(),

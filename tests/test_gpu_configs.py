@@ -116,7 +116,7 @@ def test_config_point_against_oracle(lib, name, T):
         experts = e_gpu[pos // bm]
         # gate_up + SiLU-and-mul
         h_ref = oracle.silu_mul(oracle.gemm_rows(x, k, w13_q, w13_s, slots, experts,
-                                                 threads=THREADS))
+                                                 out_f32=True, threads=THREADS))
         h_pos = h[torch.from_numpy(pos).to(DEV)].cpu()
         assert_close_bf16(h_pos, h_ref, f"{name} T={T} gate_up rows ({pos.size} of {n_routed})")
         # down, on the CUDA path's own gate_up rows

@@ -39,7 +39,7 @@ def test_pairs_match_oracle_and_single_cta(lib, mode, paired, epilogue):
     kw = dict(epilogue=epilogue, row_flags=lib.A_ROWS_SORTED)
     one = lib.moe_gemm(xs, 1, W, r, cta_pairs=1, **kw).cpu()
     two = lib.moe_gemm(xs, 1, W, r, cta_pairs=mode, **kw).cpu()
-    ref = oracle.moe_gemm(x, k, qw, sc, s, e, ntp, 128, T * k)
+    ref = oracle.moe_gemm(x, k, qw, sc, s, e, ntp, 128, T * k, out_f32=bool(epilogue))
     if epilogue:
         ref = oracle.silu_mul(ref)
     rows = routed_rows(ids)
@@ -56,7 +56,7 @@ def test_pairs_odd_k_tail(lib, mode):
     kw = dict(epilogue=1, row_flags=lib.A_ROWS_SORTED)
     one = lib.moe_gemm(xs, 1, W, r, cta_pairs=1, **kw).cpu()
     two = lib.moe_gemm(xs, 1, W, r, cta_pairs=mode, **kw).cpu()
-    ref = oracle.silu_mul(oracle.moe_gemm(x, k, qw, sc, s, e, ntp, 128, T * k))
+    ref = oracle.silu_mul(oracle.moe_gemm(x, k, qw, sc, s, e, ntp, 128, T * k, out_f32=True))
     rows = routed_rows(ids)
     assert_close_bf16(two[rows], ref[rows], f"pairs mode {mode}, K tail")
     assert torch.equal(bits(two[rows]), bits(one[rows]))
@@ -105,7 +105,8 @@ def test_pairs_qwen3_prefill_sampled_rows(lib, mode):
     pos = torch.nonzero(torch.from_numpy(s[:ntp]) < T * wl.top_k).reshape(-1)[::97]
     slots = torch.from_numpy(s[pos.numpy()]).long()
     experts = torch.from_numpy(e[(pos // 128).numpy()]).long()
-    ref = oracle.silu_mul(oracle.gemm_rows(x, wl.top_k, qw, sc, slots.numpy(), experts.numpy()))
+    ref = oracle.silu_mul(oracle.gemm_rows(x, wl.top_k, qw, sc, slots.numpy(), experts.numpy(),
+                                           out_f32=True))
     assert_close_bf16(C[pos], ref, f"qwen3 T=4096 pairs mode {mode}")
 
 

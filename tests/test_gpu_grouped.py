@@ -36,7 +36,7 @@ def test_contiguous_matches_oracle(lib, epilogue):
     x, mi = contiguous_layout([(0, 5), (3, 128), (1, 200), (7, 300), (2, 1)], seed=31, K=K)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     out = lib.contiguous_gemm(x.to(DEV), W, mi.to(DEV), epilogue=epilogue, dev_err=err).cpu()
-    ref = oracle.contiguous_gemm(x, qw, sc, mi)
+    ref = oracle.contiguous_gemm(x, qw, sc, mi, out_f32=bool(epilogue))
     if epilogue:
         ref = oracle.silu_mul(ref)
     valid = mi >= 0
@@ -55,7 +55,8 @@ def test_contiguous_qwen_shape_from_a_routing(lib):
     x, mi = contiguous_layout([(e, c) for e, c in enumerate(counts) if c], seed=32, K=wl.H)
     out = lib.contiguous_gemm(x.to(DEV), W, mi.to(DEV), epilogue=1).cpu()
     rows = torch.nonzero(mi >= 0).reshape(-1)[::7]  # a sample of the valid rows
-    ref = oracle.silu_mul(oracle.gemm_rows(x, 1, qw, sc, rows.numpy(), mi[rows].numpy()))
+    ref = oracle.silu_mul(oracle.gemm_rows(x, 1, qw, sc, rows.numpy(), mi[rows].numpy(),
+                                           out_f32=True))
     assert_close_bf16(out[rows], ref, "contiguous qwen rows")
 
 
@@ -87,7 +88,7 @@ def test_masked_silu_and_two_calls_identical(lib):
     mm = torch.arange(G, dtype=torch.int32) * 2
     a = lib.masked_gemm(x.to(DEV), W, mm.to(DEV), 8, epilogue=1).cpu()
     b = lib.masked_gemm(x.to(DEV), W, mm.to(DEV), 8, epilogue=1).cpu()
-    ref = oracle.silu_mul(oracle.masked_gemm(x, qw, sc, mm, max_m))
+    ref = oracle.silu_mul(oracle.masked_gemm(x, qw, sc, mm, max_m, out_f32=True))
     valid = (torch.arange(max_m)[None, :] < mm[:, None].long()).reshape(-1)
     assert_close_bf16(a[valid], ref[valid], "masked silu")
     assert torch.equal(bits(a[valid]), bits(b[valid]))

@@ -76,7 +76,7 @@ def test_nvfp4_gemm_matches_oracle(lib, bm, epilogue):
     r = lib.moe_align(ids.to(DEV), E, bm)
     got = lib.moe_gemm(x.to(DEV), k, W, r, epilogue=epilogue).cpu()
     s, e, ntp = oracle.moe_align(ids, E, bm)
-    ref = oracle.nvfp4_moe_gemm(x, k, codes, scales, s, e, ntp, bm, T * k)
+    ref = oracle.nvfp4_moe_gemm(x, k, codes, scales, s, e, ntp, bm, T * k, out_f32=bool(epilogue))
     if epilogue:
         ref = oracle.silu_mul(ref)
     rows = routed_rows(ids)
@@ -87,7 +87,7 @@ def _oracle_nvfp4_layer(x, w13, w2, ids, tw, bm):
     T, k = ids.shape
     E = w13[0].shape[0]
     s, e, ntp = oracle.moe_align(ids, E, bm)
-    c13 = oracle.nvfp4_moe_gemm(x, k, *w13, s, e, ntp, bm, T * k)
+    c13 = oracle.nvfp4_moe_gemm(x, k, *w13, s, e, ntp, bm, T * k, out_f32=True)
     h = oracle.silu_mul(c13)
     y = oracle.nvfp4_moe_gemm(h, 1, *w2, s, e, ntp, bm, T * k, out_f32=True)
     return oracle.topk_sum(y, ids, tw)

@@ -155,7 +155,7 @@ def test_gemm_silu_and_none_epilogues_with_paired_layout(lib, paired):
     C = lib.moe_gemm(x.to(DEV), 4, W, r)
     assert_close_bf16(C.cpu()[rows], ref_c[rows], "gate_up (paired, NONE)")
     H = lib.moe_gemm(x.to(DEV), 4, W, r, epilogue=lib.EPILOGUE_SILU_MUL)
-    ref_h = oracle.silu_mul(ref_c)
+    ref_h = oracle.silu_mul(oracle.moe_gemm(x, 4, qw, sc, s, e, ntp, 16, 160, out_f32=True))
     assert_close_bf16(H.cpu()[rows], ref_h[rows], "gate_up + SiLU-mul")
 
 

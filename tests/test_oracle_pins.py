@@ -392,6 +392,17 @@ def test_silu_mul_against_scipy_and_odd_identity():
     # silu(0) = 0
     z = torch.zeros((1, 2), dtype=torch.bfloat16)
     assert float(oracle.silu_mul(z)[0, 0]) == 0.0
+    # FP32 gate/up sums (not BF16 values) are used as they are: one rounding, of h
+    g32 = (rng.standard_normal(4000) * 4).astype(np.float32)
+    u32 = rng.standard_normal(4000).astype(np.float32)
+    h32 = bf16_np(oracle.silu_mul(torch.from_numpy(np.stack([g32, u32], 1))))[:, 0]
+    g64, u64 = g32.astype(np.float64), u32.astype(np.float64)
+    ref32 = g64 * expit(g64) * u64
+    assert np.all(np.abs(h32 - ref32) <= 0.5 * ulp_bf16(ref32) + 1e-30)
+    # a gate/up pair that BF16 would move: the unrounded up value decides h
+    gu = torch.tensor([[1.0, 1.00390625 + 2.0 ** -10]], dtype=torch.float32)  # up between two BF16s
+    assert float(oracle.silu_mul(gu)[0, 0]) == float(torch.tensor(
+        0.7310585786300049 * (1.00390625 + 2.0 ** -10)).to(torch.bfloat16))
 
 
 def test_topk_sum_brute_force_and_special_cases():
@@ -442,8 +453,9 @@ def _round_bf16_exact(v: Fraction) -> float:
 # ---- whole layer --------------------------------------------------------------------
 
 def _layer_brute(inp):
-    """Per-token loops in numpy float64, BF16 rounding at the gate_up, SiLU-mul and final
-    outputs (the per-slot down outputs are summed unrounded)."""
+    """Per-token loops in numpy float64, BF16 rounding at the SiLU-mul and final outputs (the
+    gate_up sums feed SiLU-and-mul unrounded; the per-slot down outputs are summed
+    unrounded)."""
     from scipy.special import expit
     wl = inp.wl
     w13 = dequant_np(inp.w13_q.numpy(), inp.w13_s.view(torch.int16).numpy())
@@ -461,7 +473,7 @@ def _layer_brute(inp):
             ex = int(inp.topk_ids[t, s])
             if ex < 0:
                 continue
-            c = rb(w13[ex] @ xa[t])
+            c = w13[ex] @ xa[t]
             g, u = c[: wl.I], c[wl.I:]
             h = rb(g * expit(g) * u)
             y = w2[ex] @ h  # per-slot down output stays unrounded until the weighted sum

@@ -184,10 +184,6 @@ __device__ __forceinline__ bool epi_any(bool pred) {
   return out != 0;
 }
 
-__device__ __forceinline__ float bf16_round(float x) {
-  return __bfloat162float(__float2bfloat16_rn(x));
-}
-
 // 256-bit global stores (sm_100 and later; the address must be 32-byte aligned).
 __device__ __forceinline__ void st_global_v8(float* p, float4 x, float4 y) {
   asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(x.x),
@@ -219,14 +215,16 @@ __device__ __forceinline__ void store_chunk16(const GemmArgs& a, const Unit& un,
   if (a.epilogue == W4A16_EPILOGUE_SILU_MUL) {
     // Lane l < 16 holds gate rows and lane l + 16 the matching up rows.  For each pair of
     // tokens (j, j + 1) one exchange lets lane l compute token j and lane l + 16 token j + 1.
+    // SiLU-and-mul takes the FP32 sums as they leave the accumulator (no BF16 gate_up tensor
+    // exists between the two GEMMs); h is rounded to BF16 once.
     uint16_t* st = reinterpret_cast<uint16_t*>(stage);  // [16 tokens][16 columns]
     const bool hi = lane >= 16;
 #pragma unroll
     for (int jj = 0; jj < 16; jj += 2) {
       const float v0 = __uint_as_float(r[jj]), v1 = __uint_as_float(r[jj + 1]);
       const float recv = __shfl_xor_sync(0xffffffffu, hi ? v0 : v1, 16);
-      const float g = bf16_round(hi ? recv : v0);
-      const float u = bf16_round(hi ? v1 : recv);
+      const float g = hi ? recv : v0;
+      const float u = hi ? v1 : recv;
       const float h = __fdividef(g, 1.0f + __expf(-g)) * u;
       st[(jj + (hi ? 1 : 0)) * 16 + (lane & 15)] = __bfloat16_as_ushort(__float2bfloat16_rn(h));
     }
