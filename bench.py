@@ -63,7 +63,14 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 DECODE_ROOFLINE_T = 64
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum from an ncu capture of
 # that launch), valid only while the GEMM kernel's sources hash to the recorded value.
-ROOFLINE_TRAFFIC = {}
+# Captured with `bench.py --profile-call <proj> --workload qwen3_30b_a3b --tokens <T> --repeat 3`
+# under `ncu --set full -k regex:moe_gemm -s 2 -c 1` (L2 flushed before each call).
+_SRC_SHA = "3764b5f98bd35912c6571d19030855b005cecbca73fad712360d2332fd8a5f81"
+ROOFLINE_TRAFFIC = {
+    "gate_up_T4096": {"bytes": 392440320 + 51900928, "sources_sha256": _SRC_SHA},
+    "down_T4096": {"bytes": 175635968 + 218235648, "sources_sha256": _SRC_SHA},
+    "gate_up_T64": {"bytes": 223307776 + 3919616, "sources_sha256": _SRC_SHA},
+}
 GEMM_SOURCES = ("w4a16_moe_expert_gb300/csrc/gemm.cu", "w4a16_moe_expert_gb300/csrc/gemm.cuh",
                 "w4a16_moe_expert_gb300/csrc/common.cuh")
 
@@ -872,6 +879,59 @@ def run_reference(args, rank, world, local_rank):
     }
 
 
+def run_profile_call(args):
+    """One projection of one workload point, called --repeat times with a 256 MB L2 flush
+    before each call, for an ncu capture of its last launch (``-k regex:moe_gemm``: only the
+    profiled projection launches the GEMM kernel; the down projection reads random BF16 rows
+    in place of a gate_up output).  Prints one line naming the schedule."""
+    import w4a16_moe_expert_gb300 as lib
+    from w4a16_moe_expert_gb300 import workloads
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    lib.load()
+    wl = workloads.WORKLOADS[args.workload]
+    T = int(args.tokens)
+    q, s, q2, s2 = workloads.draw_layer_weights(wl)
+    if args.profile_call == "gate_up":
+        W = lib.pack_weights(q.to(dev), s.to(dev), paired=True)
+    else:
+        W = lib.pack_weights(q2.to(dev), s2.to(dev))
+    del q, s, q2, s2
+    x, ids, _ = workloads.draw_layer_routing(wl, T)
+    bm = lib.plan_block_m(T, wl.top_k, wl.E, wl.E_global)
+    r = lib.moe_align(ids.to(dev), wl.E, bm)
+    hint = max(1, round(T * wl.top_k / wl.E_global))
+    ws = lib.gemm_workspace(T * wl.top_k, wl.E, W.N, W.K, bm, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    kw = dict(workspace=ws, expected_rows_per_expert=hint, split_k=args.split, num_ctas=0)
+    if args.profile_call == "gate_up":
+        if bm >= 64:
+            A, div = lib.gather_rows(x.to(dev), wl.top_k, r), 1
+            kw["row_flags"] = lib.A_ROWS_SORTED | lib.C_ROWS_SORTED
+        else:
+            A, div = x.to(dev), wl.top_k
+            kw["row_flags"] = lib.C_ROWS_SORTED
+        kw["epilogue"] = lib.EPILOGUE_SILU_MUL
+    else:
+        g = torch.Generator(device=dev).manual_seed(T)
+        A = torch.randn((r.capacity, wl.I), generator=g, device=dev).to(torch.bfloat16)
+        div = 1
+        kw["row_flags"] = lib.A_ROWS_SORTED | lib.C_FP32
+    out = None
+    for _ in range(args.repeat):
+        flush.zero_()
+        out = lib.moe_gemm(A, div, W, r, out=out, **kw)
+    torch.cuda.synchronize()
+    n_slots = T * wl.top_k
+    plan = lib.plan_gemm(n_slots, wl.E, W.N, W.K, bm, num_sms=torch.cuda.get_device_properties(
+        dev).multi_processor_count, expected_rows_per_expert=hint)
+    print(json.dumps({"profile_call": args.profile_call, "workload": wl.name, "T": T,
+                      "block_m": bm, "split_k_arg": args.split, "plan": plan,
+                      "num_tokens_padded": int(r.num_tokens_padded.item()),
+                      "launches": args.repeat}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -888,7 +948,15 @@ def main():
                     help="skip the NVFP4, grouped-contract and CTA-pair measurements")
     ap.add_argument("--no-other-configs", action="store_true",
                     help="skip the Kimi-K2 EP8 decode / EP8 prefill / TP8 sweeps")
+    ap.add_argument("--profile-call", choices=["gate_up", "down"], default=None,
+                    help="run only this projection of --workload at --tokens (one T), --repeat "
+                         "times, for an ncu capture; prints no bench line")
+    ap.add_argument("--repeat", type=int, default=3)
+    ap.add_argument("--split", type=int, default=0, help="--profile-call: fixed K split (0: planner)")
     args = ap.parse_args()
+    if args.profile_call:
+        run_profile_call(args)
+        return
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps are required")
     rank, world, local_rank = dist_env()

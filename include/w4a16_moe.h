@@ -157,14 +157,20 @@ w4a16_status_t w4a16_pack_weights_nvfp4(const uint8_t* codes, const uint8_t* sca
  * A  device BF16 [rows, K] with row stride lda elements (lda % 8 == 0, 16-byte aligned rows).
  * C  device BF16 (16-byte aligned, ldc % 8 == 0; FP32: ldc % 4 == 0) with row stride ldc
  *    elements; N columns (epilogue NONE) or N/2 columns
- *    (epilogue SILU_MUL: C[., j] = bf16(silu(g) * u), g and u the BF16-rounded gate and up
- *    outputs; needs a W4A16_PACK_GATE_UP_PAIRED weight).
+ *    (epilogue SILU_MUL: C[., j] = bf16(silu(g) * u), g and u the unrounded FP32 gate and up
+ *    sums; needs a W4A16_PACK_GATE_UP_PAIRED weight).
  * workspace  device scratch of w4a16_gemm_workspace_size() bytes, 256-byte aligned; its
  *    counter words must be zero before the first use (w4a16_workspace_clear, or cudaMemset)
  *    and every call leaves them zero.  Concurrent calls must not share a workspace.
  * expected_rows_per_expert  host hint for the schedule (0: total_slots / E); it never
  *    changes results, which are independent of the schedule up to FP32 summation order
  *    (and bitwise identical between runs of the same schedule).
+ * Schedule: unless `schedule` fixes split_k, the K split of a tile is picked on the device
+ *    from *num_tokens_padded: when the routed (block, 128-row tile) units are fewer than half
+ *    the CTAs, K is sliced (at most 8 slices of at least 1536 K elements) so that the units
+ *    fill one wave; the slices' FP32 partials are summed in slice order by the last CTA to
+ *    finish the tile (deterministic).  Without a workspace large enough for the partials
+ *    tiles are never split.
  * ---------------------------------------------------------------------------------------- */
 #define W4A16_EPILOGUE_NONE 0
 #define W4A16_EPILOGUE_SILU_MUL 1
@@ -349,7 +355,7 @@ w4a16_status_t w4a16_moe_layer_ex(const uint16_t* x, const w4a16_packed_weights_
  * ---------------------------------------------------------------------------------------- */
 typedef struct {
   int32_t block_m;
-  int32_t split_k;
+  int32_t split_k;     /* most K slices per tile the device may pick (see w4a16_moe_gemm) */
   int32_t num_ctas;
   int32_t stages;      /* weight/activation ring depth in shared memory */
   int32_t est_units;   /* estimated (block, tile, split) work units */

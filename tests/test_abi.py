@@ -69,12 +69,22 @@ def test_block_m_planner():
 
 
 def test_gemm_planner_grid_and_split():
-    # decode: 8 routed rows over 128 experts -> ~8 blocks x 12 tiles = 96 units, one CTA each
+    # decode, K = 2048 (32 blocks of 64) is never split (a slice keeps at least 24 blocks):
+    # 8 routed rows over 128 experts -> ~8 blocks x 12 tiles = 96 units, one CTA each
     p = lib.plan_gemm(8, 128, 1536, 2048, 16, num_sms=148)
     assert p["split_k"] == 1 and p["num_ctas"] == 96 and p["est_units"] == 96
+    # Kimi-K2 gate_up, K = 7168 (112 blocks): the device may take up to 4 slices, so the grid
+    # is one CTA per SM
+    p = lib.plan_gemm(8, 48, 4096, 7168, 16, num_sms=148)
+    assert p["split_k"] == 4 and p["num_ctas"] == 148
+    # at most 8 slices
+    assert lib.plan_gemm(8, 48, 4096, 16384, 16, num_sms=148)["split_k"] == 8
+    # K = 768 (12 blocks) is never split: the grid covers the estimated units
+    p = lib.plan_gemm(8, 128, 2048, 768, 16, num_sms=148)
+    assert p["split_k"] == 1 and p["num_ctas"] == min(148, p["est_units"]) == 128
     # prefill: thousands of tiles, a persistent grid of one CTA per SM
     p = lib.plan_gemm(32768, 128, 1536, 2048, 128, num_sms=148)
-    assert p["split_k"] == 1 and p["num_ctas"] == 148
+    assert p["num_ctas"] == 148
     assert p["stages"] >= 4
     with pytest.raises(lib.LibraryError):
         lib.plan_gemm(8, 128, 1536, 2000, 16, num_sms=148)

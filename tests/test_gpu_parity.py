@@ -179,6 +179,37 @@ def test_gemm_split_k_parity_and_determinism(lib, split):
     assert torch.equal(bits(C1), bits(C2)), "same schedule must be bitwise reproducible"
 
 
+@pytest.mark.parametrize("epilogue", [0, 1])
+def test_gemm_device_picked_split_for_few_long_tiles(lib, epilogue):
+    # One routed row on a wide, long-K weight: 32 tiles of K = 6144 leave most SMs idle, so the
+    # device slices K until the units fill one wave (at most 8 slices of >= 24 K blocks).  The
+    # result matches the oracle and, bit for bit, the same split fixed by the schedule.
+    E, N, K = 4, 4096, 6144
+    qw, sc, x, ids, W, r, (s, e, ntp) = _gemm_case(lib, 1, 1, E, N, K, 16, 41, paired=True)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    units1 = (ntp // 16) * (N // 128)
+    split = min(8, sms // units1)
+    while split > 1 and K // 64 < 24 * split:
+        split -= 1
+    assert split > 1
+    auto = lib.moe_gemm(x.to(DEV), 1, W, r, epilogue=epilogue)
+    fixed = lib.moe_gemm(x.to(DEV), 1, W, r, epilogue=epilogue, split_k=split, num_ctas=sms)
+    ref = oracle.moe_gemm(x, 1, qw, sc, s, e, ntp, 16, 1, out_f32=bool(epilogue))
+    if epilogue:
+        ref = oracle.silu_mul(ref)
+    assert_close_bf16(auto.cpu(), ref, f"device-picked split ({split})")
+    assert torch.equal(bits(auto), bits(fixed))
+
+
+def test_gemm_units_filling_the_grid_are_not_split(lib):
+    # 64 tokens x 8 slots over 128 experts: hundreds of (block, tile) units, so no K split
+    qw, sc, x, ids, W, r, (s, e, ntp) = _gemm_case(lib, 64, 8, 128, 1536, 2048, 16, 42)
+    auto = lib.moe_gemm(x.to(DEV), 8, W, r)
+    one = lib.moe_gemm(x.to(DEV), 8, W, r, split_k=1,
+                       num_ctas=torch.cuda.get_device_properties(0).multi_processor_count)
+    assert torch.equal(bits(auto), bits(one))
+
+
 def test_gemm_grid_sizes_do_not_change_results(lib):
     qw, sc, x, ids, W, r, (s, e, ntp) = _gemm_case(lib, 64, 8, 128, 512, 512, 16, 23)
     outs = [lib.moe_gemm(x.to(DEV), 8, W, r, num_ctas=n, split_k=1) for n in (1, 7, 64, 1000)]

@@ -285,15 +285,21 @@ static w4a16_status_t prepare_gemm(const GemmCall& c, const DeviceFacts& dev, Ge
   plan_gemm(R->total_slots, c.W->E, c.W->N, c.W->K, R->block_m, c.rows_hint, dev.num_sms, &plan);
   int split = plan.split_k, grid = plan.num_ctas;
   const int n_kb = c.W->K / kBlockK;
-  if (c.sched && c.sched->split_k > 0) split = c.sched->split_k;
+  // an explicit split is taken as given; the planner's is an upper bound for the device
+  const bool split_fixed = c.sched && c.sched->split_k > 0;
+  if (split_fixed) split = c.sched->split_k;
   if (c.sched && c.sched->num_ctas > 0) grid = c.sched->num_ctas;
   split = std::max(1, std::min(split, std::min(16, n_kb)));
   grid = std::max(1, std::min(grid, dev.num_sms));
 
   const int64_t budget = split_unit_budget(R->block_m);
   const size_t cnt_bytes = round_up(static_cast<size_t>(budget) * sizeof(int32_t), 256);
-  if (split > 1 && (!c.ws || c.ws_bytes < cnt_bytes + kPartialBytes))
-    return fail(W4A16_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes", cnt_bytes + kPartialBytes);
+  const bool have_scratch = c.ws && c.ws_bytes >= cnt_bytes + kPartialBytes;
+  if (split > 1 && !have_scratch) {
+    if (split_fixed)
+      return fail(W4A16_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes", cnt_bytes + kPartialBytes);
+    split = 1;  // no scratch for partial sums: whole-K tiles
+  }
 
   GemmArgs& a = *out;
   std::memset(&a, 0, sizeof a);
@@ -326,6 +332,7 @@ static w4a16_status_t prepare_gemm(const GemmCall& c, const DeviceFacts& dev, Ge
   a.cnt = static_cast<int32_t*>(c.ws);
   a.part = c.ws ? reinterpret_cast<float*>(static_cast<uint8_t*>(c.ws) + cnt_bytes) : nullptr;
   a.split_k = split;
+  a.split_auto = (!split_fixed && split > 1) ? 1 : 0;
   a.max_split_units = budget;
   a.dev_err = c.dev_err;
   // weights streamed once per call (few rows per expert) are marked evict-first in L2
@@ -334,8 +341,8 @@ static w4a16_status_t prepare_gemm(const GemmCall& c, const DeviceFacts& dev, Ge
   a.merge_w = c.merge_w;
   a.merge_k = c.merge_k;
   // CTA pairs (one M = 256 MMA over two CTAs' tiles) for 128-token blocks of sorted rows
-  const bool pair_ok = R->block_m == 128 && a.a_sorted && split == 1 && a.n_tiles % 2 == 0 &&
-                       grid >= 2 && !c.merge_w;
+  const bool pair_ok = R->block_m == 128 && a.a_sorted && (split == 1 || a.split_auto) &&
+                       a.n_tiles % 2 == 0 && grid >= 2 && !c.merge_w;
   const int want_pair = c.sched ? c.sched->cta_pairs : 0;
   if (want_pair < 0 || want_pair > 2)
     return fail(W4A16_INVALID_ARG, "cta_pairs %d: supported values are 0, 1, 2", want_pair);
@@ -343,7 +350,9 @@ static w4a16_status_t prepare_gemm(const GemmCall& c, const DeviceFacts& dev, Ge
     return fail(W4A16_INVALID_ARG, "CTA pairs need block_m 128, sorted activation rows, an even "
                                    "tile count and no K split");
   a.pair = (want_pair == 2 || (want_pair == 0 && pair_ok && kPairsByDefault)) ? 1 : 0;
-  if (a.pair) {
+  if (a.pair) {  // whole-K tiles
+    a.split_k = 1;
+    a.split_auto = 0;
     grid &= ~1;
     fast_divisor(static_cast<uint32_t>(a.n_tiles / 2), &a.nt2_magic, &a.nt2_shift);
   }

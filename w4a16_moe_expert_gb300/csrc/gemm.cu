@@ -430,8 +430,19 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
   if (ntp < 0) ntp = 0;
   if (ntp > a.capacity) ntp = static_cast<int>(a.capacity);
   const int64_t nblocks = ntp / a.block_m;
-  // Fewer K splits when the routed blocks would overflow the partial-sum scratch.
+  // Decode schedule from the routed blocks: when the (block, tile) units leave SMs idle, each
+  // tile's K range is sliced so that the units fill one wave (every role computes the same
+  // count from num_tokens_padded).  Fewer K splits when the routed blocks would overflow the
+  // partial-sum scratch.
   int split_k = a.split_k;
+  if (a.split_auto) {
+    const int64_t units1 = nblocks * a.n_tiles;
+    int s = units1 > 0 ? static_cast<int>(min(static_cast<int64_t>(split_k),
+                                              static_cast<int64_t>(gridDim.x) / units1))
+                       : 1;
+    while (s > 1 && a.n_kb < s * kMinSplitKb) --s;
+    split_k = s > 1 ? s : 1;
+  }
   while (split_k > 1 && nblocks * a.n_tiles * split_k > a.max_split_units) --split_k;
   const int64_t units0 = CL ? nblocks * (a.n_tiles >> 1) : nblocks * a.n_tiles * split_k;
   const int64_t n_units = FUSED ? units0 + nblocks * a2.n_tiles : units0;
@@ -995,34 +1006,23 @@ double expected_blocks(int total_slots, int E, int block_m, double rows_per_expe
   return std::min(active * per, static_cast<double>(total_slots));
 }
 
-// Split-K choice: minimise the busiest CTA's bytes, ceil(units * S / P) * (W / S + R), where W
-// is one tile's packed weight bytes and R the FP32 partial round trip a split adds.
+// Split-K: the split itself is chosen on the device from the routed block count (the host
+// cannot know it without a read-back).  The planner allows it where a slice keeps at least
+// kMinSplitKb K blocks and then launches one CTA per SM, so that a call whose routed units
+// leave SMs idle (one or a few experts with long K at decode, e.g. 32 tiles of K = 7168) can
+// slice K until the units fill the grid.  Where the units fill the grid no split happens:
+// measured on GB300, a second wave of half-length units plus the partial round trip is
+// slower than one wave of whole ones (Qwen3 T=1 gate_up, 96 units: 7.9 -> 11.1 us).
 void plan_gemm(int total_slots, int E, int N, int K, int block_m, int rows_per_expert,
                int num_sms, w4a16_plan_t* plan) {
   const int n_tiles = N / kTileRows, n_kb = K / kBlockK;
   const double blocks = expected_blocks(total_slots, E, block_m, rows_per_expert);
   const double units1 = std::max(1.0, std::ceil(blocks)) * n_tiles;
-  const double W = static_cast<double>(n_kb) * kChunkBytes;
-  const double R = 2.0 * 128 * block_m * 4;
-  // K splits measured slower than unsplit units at every decode size on GB300 (the partial
-  // round trip and the extra per-unit pipeline ramp outweigh the added parallelism), so the
-  // planner keeps one split; the schedule override still exercises the split path.
-  const int s_max = 1;
-  (void)n_kb;
-  int best_s = 1;
-  double best = 1e300;
-  for (int s = 1; s <= s_max; ++s) {
-    const double waves = std::ceil(units1 * s / num_sms);
-    const double cost = waves * (W / s + (s > 1 ? R : 0.0));
-    if (cost < best * 0.97) {  // prefer fewer splits unless clearly better
-      best = cost;
-      best_s = s;
-    }
-  }
+  const int split_max = std::max(1, std::min(kMaxAutoSplit, n_kb / kMinSplitKb));
   plan->block_m = block_m;
-  plan->split_k = best_s;
-  plan->est_units = static_cast<int32_t>(std::min(units1 * best_s, 2.0e9));
-  plan->num_ctas = std::max(1, std::min(num_sms, plan->est_units));
+  plan->split_k = split_max;
+  plan->est_units = static_cast<int32_t>(std::min(units1, 2.0e9));
+  plan->num_ctas = split_max > 1 ? num_sms : std::max(1, std::min(num_sms, plan->est_units));
   plan->stages = stages_for_block_m(block_m);
 }
 

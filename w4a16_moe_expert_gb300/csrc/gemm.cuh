@@ -36,6 +36,9 @@ struct GemmArgs {
   float* part;
   int32_t* cnt;
   int split_k;
+  // split_k is an upper bound: the device takes as many K slices as keep the routed
+  // (block, tile) units within one wave of the grid, each slice at least kMinSplitKb K blocks
+  int split_auto;
   int64_t max_split_units;  // K splits are reduced on the device until units fit the scratch
   int32_t* dev_err;
   int evict_first;
@@ -57,6 +60,14 @@ struct GemmArgs {
   int pair;
   uint32_t nt2_magic, nt2_shift;
 };
+
+// Fewest 64-wide K blocks one K slice of an automatically split tile streams (1536 K elements:
+// six pipeline stages at decode block sizes).  Measured on GB300: slicing K = 2048 in two
+// (Kimi-K2 EP8 down at T=1, 56 tiles -> 112 units) is slower (7.5 -> 8.3 us), slicing
+// K = 7168 in four (32 tiles -> 128 units) much faster (gate_up 16.3 -> 10.5 us).
+constexpr int kMinSplitKb = 24;
+// Most K slices the planner lets the device choose.
+constexpr int kMaxAutoSplit = 8;
 
 // The fused layer call: gate_up (a) then down (a2) in one cooperative persistent launch.
 cudaError_t launch_layer_fused(GemmArgs& a, GemmArgs& a2, int grid, cudaStream_t stream);
