@@ -194,6 +194,10 @@ typedef struct {
   int32_t cta_pairs; /* 128-token blocks only: 1 = one CTA per MMA, 2 = CTA pairs (tcgen05
                         cta_group::2, M = 256 over two 128-row tiles; needs sorted activation
                         rows, an even tile count and no K split); 0 = planner */
+  int32_t tile_group; /* 128-row weight tiles per work unit: 1 = one; 2 or 4 = consecutive
+                         tiles of one block sharing its activation stages (16-token blocks up
+                         to 4, 32-token blocks up to 2, K <= 512, no K split, N / 128 a
+                         multiple); 0 = planner (the largest allowed) */
 } w4a16_schedule_t;
 
 size_t w4a16_gemm_workspace_size(int total_slots, int E, int N, int K, int block_m);

@@ -69,7 +69,8 @@ class RoutingDesc(ctypes.Structure):
 
 
 class ScheduleDesc(ctypes.Structure):
-    _fields_ = [("split_k", ctypes.c_int32), ("num_ctas", ctypes.c_int32), ("cta_pairs", ctypes.c_int32)]
+    _fields_ = [("split_k", ctypes.c_int32), ("num_ctas", ctypes.c_int32), ("cta_pairs", ctypes.c_int32),
+                ("tile_group", ctypes.c_int32)]
 
 
 class PlanDesc(ctypes.Structure):
@@ -307,10 +308,12 @@ def moe_gemm(A: torch.Tensor, a_row_div: int, W: PackedWeights, routing: Routing
              epilogue: int = EPILOGUE_NONE, row_flags: int = 0, out: Optional[torch.Tensor] = None,
              out_rows: Optional[int] = None, workspace: Optional[torch.Tensor] = None,
              expected_rows_per_expert: int = 0, split_k: int = 0, num_ctas: int = 0,
-             dev_err: Optional[torch.Tensor] = None, cta_pairs: int = 0) -> torch.Tensor:
-    """The indexed W4A16 GEMM (``w4a16_moe_gemm``).  ``split_k``, ``num_ctas`` and
-    ``cta_pairs`` override the planner for measurements (0 = planner; cta_pairs 1 = one CTA per
-    128-row tile, 2 = one M = 256 MMA over two CTAs)."""
+             dev_err: Optional[torch.Tensor] = None, cta_pairs: int = 0,
+             tile_group: int = 0) -> torch.Tensor:
+    """The indexed W4A16 GEMM (``w4a16_moe_gemm``).  ``split_k``, ``num_ctas``, ``cta_pairs``
+    and ``tile_group`` override the planner for measurements (0 = planner; cta_pairs 1 = one
+    CTA per 128-row tile, 2 = one M = 256 MMA over two CTAs; tile_group 1 = one tile per work
+    unit, 2 or 4 = that many tiles of a block per unit)."""
     _cuda(A, torch.bfloat16, "A")
     width = W.N // 2 if epilogue == EPILOGUE_SILU_MUL else W.N
     if out is None:
@@ -321,7 +324,7 @@ def moe_gemm(A: torch.Tensor, a_row_div: int, W: PackedWeights, routing: Routing
     _cuda(out, torch.float32 if row_flags & C_FP32 else torch.bfloat16, "out")
     if workspace is None:
         workspace = gemm_workspace(routing.total_slots, W.E, W.N, W.K, routing.block_m, A.device)
-    sched = ScheduleDesc(split_k, num_ctas, cta_pairs)
+    sched = ScheduleDesc(split_k, num_ctas, cta_pairs, tile_group)
     rd = routing.desc()
     _check("w4a16_moe_gemm", load().w4a16_moe_gemm(
         _ptr(A), A.stride(0), a_row_div, ctypes.byref(W.desc), ctypes.byref(rd), epilogue, row_flags,

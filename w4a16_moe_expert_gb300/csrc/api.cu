@@ -236,6 +236,7 @@ struct GemmCall {
   int routing_ready;
   const float* merge_w = nullptr;  // fused top-k merge (C = FP32 token sums)
   int merge_k = 0;
+  bool one_kernel = false;  // an argument set of the single-kernel layer (one tile per unit)
 };
 
 // 128-token blocks use CTA pairs unless the schedule says otherwise.
@@ -313,7 +314,9 @@ static w4a16_status_t prepare_gemm(const GemmCall& c, const DeviceFacts& dev, Ge
   a.K = c.W->K;
   a.n_tiles = c.W->N / kTileRows;
   a.n_kb = n_kb;
-  fast_divisor(static_cast<uint32_t>(a.n_tiles), &a.nt_magic, &a.nt_shift);
+  a.tpu = 1;
+  a.n_tg = a.n_tiles;
+  fast_divisor(static_cast<uint32_t>(a.n_tg), &a.nt_magic, &a.nt_shift);
   a.paired = paired ? 1 : 0;
   a.nvfp4 = (c.W->flags & W4A16_PACK_NVFP4) ? 1 : 0;
   a.tile_mode = a.wblob + tile_mode_offset(a.E, a.n_tiles, n_kb);
@@ -355,6 +358,32 @@ static w4a16_status_t prepare_gemm(const GemmCall& c, const DeviceFacts& dev, Ge
     a.split_auto = 0;
     grid &= ~1;
     fast_divisor(static_cast<uint32_t>(a.n_tiles / 2), &a.nt2_magic, &a.nt2_shift);
+  }
+  // Tile groups: where a unit is at most two pipeline stages (K <= 512, the Kimi-K2 TP8 down
+  // projection's K = 256), consecutive 128-row tiles of one block share a unit, its
+  // activation stages and its per-unit hand-offs.
+  const int group_max = tile_group_max(R->block_m);
+  const int stage_kb = R->block_m <= 64 ? 4 : 2;
+  const bool group_ok = !a.pair && !c.merge_w && !c.one_kernel && a.split_k == 1 &&
+                        !a.split_auto && n_kb <= kGroupMaxKb && n_kb % stage_kb == 0;
+  const int want_group = c.sched ? c.sched->tile_group : 0;
+  if (want_group < 0 || want_group > 4 || want_group == 3)
+    return fail(W4A16_INVALID_ARG, "tile_group %d: supported values are 0, 1, 2, 4", want_group);
+  int tpu = 1;
+  if (want_group > 1) {
+    if (!group_ok || want_group > group_max || a.n_tiles % want_group)
+      return fail(W4A16_INVALID_ARG, "tile_group %d needs K <= 512 in whole stages, no K split, "
+                                     "N / 128 a multiple of it and block_m <= %d",
+                  want_group, want_group == 2 ? 32 : 16);
+    tpu = want_group;
+  } else if (want_group == 0 && group_ok) {
+    tpu = group_max;
+    while (tpu > 1 && a.n_tiles % tpu) tpu >>= 1;
+  }
+  if (tpu > 1) {
+    a.tpu = tpu;
+    a.n_tg = a.n_tiles / tpu;
+    fast_divisor(static_cast<uint32_t>(a.n_tg), &a.nt_magic, &a.nt_shift);
   }
   *out_grid = grid;
   return W4A16_OK;
@@ -827,9 +856,10 @@ w4a16_status_t w4a16_moe_layer_ex(const uint16_t* x, const w4a16_packed_weights_
               reinterpret_cast<uint16_t*>(y), H,
               ws + L.off_cnt, (L.off_xs - L.off_cnt), rows_hint, nullptr, dev_err, 1};
   if (one_kernel) {
-    const w4a16_schedule_t one_split{1, 0};
+    const w4a16_schedule_t one_split{1, 0, 0, 1};
     g1.sched = &one_split;
     g2.sched = &one_split;
+    g1.one_kernel = g2.one_kernel = true;
     g2.merge_w = topk_weights;
     g2.merge_k = top_k;
     GemmArgs a1, a2;

@@ -48,7 +48,7 @@ constexpr int kGatherThreads = 64;  // warps 2 and 3 gather activation rows with
 // Three independent rings: packed weights in shared memory (freed once the dequant warps hold
 // them in registers), activation tiles in shared memory (freed by the MMA commit), dequantised
 // weights in TMEM (freed by the MMA commit).
-template <int NT, int KS, bool PAIR = false>
+template <int NT, int KS, bool PAIR = false, int TPU = 1>
 struct GemmCfg {
   // B bytes of one sub-block (NT rows x 64; a CTA of a pair holds half the block's rows)
   static constexpr int kSubB = (PAIR ? NT / 2 : NT) * 128;
@@ -62,9 +62,10 @@ struct GemmCfg {
   static constexpr int kBStages = kBStagesRaw < 4 ? 4 : (kBStagesRaw > 24 ? 24 : kBStagesRaw);
   static constexpr int kWStagesRaw = (kSmemBudget - 4096 - kBStages * kBBytes) / kWBytes;
   static constexpr int kWStages = kWStagesRaw > 32 ? 32 : kWStagesRaw;
-  // TMEM: two FP32 accumulators of NT columns at [0, 2 NT), then as many dequantised A stages
-  // of KS * 32 columns as fit (a deep A ring covers the dequant -> MMA -> commit round trip).
-  static constexpr int kACol0 = (2 * NT + 31) / 32 * 32;
+  // TMEM: two FP32 accumulators of TPU * NT columns (TPU tiles per unit) at the start, then as
+  // many dequantised A stages of KS * 32 columns as fit (a deep A ring covers the dequant ->
+  // MMA -> commit round trip).
+  static constexpr int kACol0 = (2 * NT * TPU + 31) / 32 * 32;
   static constexpr int kAStagesRaw = (kTmemCols - kACol0) / (KS * 32);
   static constexpr int kAStages = kAStagesRaw > 12 ? 12 : kAStagesRaw;
   static constexpr int kBarBytes = (2 * kWStages + 2 * kBStages + 2 * kAStages + 5) * 8;
@@ -97,7 +98,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int split_k, int6
     tile = u;
     t.split = 0;
     t.kb0 = 0;
-    t.kb1 = a.n_kb;
+    t.kb1 = a.n_kb * a.tpu;  // a tile group's tiles are consecutive chunks of one strip
   } else {
     tile = u / static_cast<uint32_t>(split_k);
     t.split = static_cast<int>(u - tile * static_cast<uint32_t>(split_k));
@@ -107,7 +108,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int split_k, int6
   const uint32_t b = (__umulhi(tile, a.nt_magic) + tile) >> a.nt_shift;
   t.tile = tile;
   t.b = static_cast<int>(b);
-  t.jt = static_cast<int>(tile - b * static_cast<uint32_t>(a.n_tiles));
+  t.jt = static_cast<int>(tile - b * static_cast<uint32_t>(a.n_tg)) * a.tpu;
   t.e = __ldg(a.expert_ids + t.b);
   t.ok = t.e >= 0 && t.e < a.E;
   t.gi = 0;
@@ -331,9 +332,11 @@ __device__ __forceinline__ void arrive_handoff(uint32_t bar, bool leader, int la
   }
 }
 
-template <int NT, int KS, bool FUSED, bool PAIR = false>
+// TPU: 128-row tiles per unit (tile groups of short-K plain calls; 1 otherwise).
+template <int NT, int KS, bool FUSED, bool PAIR = false, int TPU = 1>
 __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2) {
-  using Cfg = GemmCfg<NT, KS, PAIR>;
+  using Cfg = GemmCfg<NT, KS, PAIR, TPU>;
+  static_assert(TPU == 1 || (!FUSED && !PAIR), "tile groups are for plain calls");
   // PAIR: two-CTA clusters taking the two tiles of a tile pair of one block, with one
   // cta_group::2 MMA over both CTAs.
   constexpr bool CL = PAIR;
@@ -436,16 +439,16 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
   // partial-sum scratch.
   int split_k = a.split_k;
   if (a.split_auto) {
-    const int64_t units1 = nblocks * a.n_tiles;
+    const int64_t units1 = nblocks * a.n_tg;
     int s = units1 > 0 ? static_cast<int>(min(static_cast<int64_t>(split_k),
                                               static_cast<int64_t>(gridDim.x) / units1))
                        : 1;
     while (s > 1 && a.n_kb < s * kMinSplitKb) --s;
     split_k = s > 1 ? s : 1;
   }
-  while (split_k > 1 && nblocks * a.n_tiles * split_k > a.max_split_units) --split_k;
-  const int64_t units0 = CL ? nblocks * (a.n_tiles >> 1) : nblocks * a.n_tiles * split_k;
-  const int64_t n_units = FUSED ? units0 + nblocks * a2.n_tiles : units0;
+  while (split_k > 1 && nblocks * a.n_tg * split_k > a.max_split_units) --split_k;
+  const int64_t units0 = CL ? nblocks * (a.n_tiles >> 1) : nblocks * a.n_tg * split_k;
+  const int64_t n_units = FUSED ? units0 + nblocks * a2.n_tg : units0;
   const uint32_t units0_u = static_cast<uint32_t>(units0);
 
   if (warp == 0) {
@@ -566,8 +569,10 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
           const int32_t i = __ldg(a.sorted_ids + static_cast<int64_t>(un.b) * a.block_m + (g >> 3) + 8 * j);
           arow[j] = (i >= 0 && i < a.total_slots) ? i / a.a_row_div : -1;
         }
-        for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
-          const int nsub = min(KS, un.kb1 - kb);
+        // a tile group's tiles share the block's activation stages: they are loaded once
+        const int kb_end = TPU > 1 ? a.n_kb : un.kb1;
+        for (int kb = un.kb0; kb < kb_end; kb += KS, ++it) {
+          const int nsub = min(KS, kb_end - kb);
           const int s = it % S_B;
           const uint32_t ph = (it / S_B) & 1;
           if (!wait_bar<PAIR>(smem_u32(&bempty[s]), ph ^ 1, abort_flag, a.dev_err)) goto bprod_done;
@@ -593,8 +598,9 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       for (int64_t u = CL ? unit0 : blockIdx.x; u < n_units; u += CL ? ustride : gridDim.x) {
         const Unit un = decode_any<FUSED, CL>(a, a2, split_k, units0_u, crank, u);
         if (!un.ok) continue;
-        for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
-          const int nsub = min(KS, un.kb1 - kb);
+        const int kb_end = TPU > 1 ? a.n_kb : un.kb1;  // tile groups: loaded once
+        for (int kb = un.kb0; kb < kb_end; kb += KS, ++it) {
+          const int nsub = min(KS, kb_end - kb);
           const int s = it % S_B;
           const uint32_t ph = (it / S_B) & 1;
           if (!__all_sync(0xffffffffu, wait_bar<PAIR>(smem_u32(&bempty[s]), ph ^ 1, abort_flag, a.dev_err)))
@@ -640,7 +646,8 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
         wait_bar_plain<PAIR>(smem_u32(drain), 0);
       }
     } else if (elect_one()) {
-      uint32_t it = 0, lu = 0;
+      uint32_t it = 0, itb = 0, lu = 0;  // A ring, activation ring, accumulator positions
+      constexpr int tpu = TPU;
       for (int64_t u = CL ? unit0 : blockIdx.x; u < n_units; u += CL ? ustride : gridDim.x) {
         const Unit un = decode_any<FUSED, CL>(a, a2, split_k, units0_u, crank, u);
         if (!un.ok) continue;
@@ -649,57 +656,73 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
         const uint32_t pab = (lu >> 1) & 1;
         if (!wait_bar<PAIR>(smem_u32(&accempty[ab]), pab ^ 1, abort_flag, a.dev_err)) goto mma_done;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + ab * NT;
+        // a tile group's tiles accumulate side by side: buffer ab holds tpu * NT columns
+        const uint32_t d_tmem = tmem_base + ab * (NT * tpu);
         // A stage's release (the commits to its two "empty" barriers) is issued only after the
         // next stage's operands are seen ready, just before that stage's MMAs: measured on GB300
         // a wait issued right after the commits costs ~3% at decode.  The commits still follow
-        // the stage's own MMAs, so they track exactly those.
+        // the stage's own MMAs, so they track exactly those.  The tiles of a group read the
+        // block's activation stages in turn; a stage is released after the last tile's MMAs.
         int prev_sbi = -1, prev_sa = 0;
+        bool prev_rel_b = true;
+        int bs = 0;  // activation stage of this K stage within the unit (per tile in a group)
+        int tg = 0;  // tile of the group
         for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
           const int nsub = min(KS, un.kb1 - kb);
-          const int sbi = it % S_B;
-          const uint32_t pb = (it / S_B) & 1;
+          const uint32_t jb = itb + static_cast<uint32_t>(bs);
+          const int sbi = jb % S_B;
+          const uint32_t pb = (jb / S_B) & 1;
           const int sa = it % S_A;
           const uint32_t pa = (it / S_A) & 1;
           if (!wait_bar<PAIR>(smem_u32(&afull[sa]), pa, abort_flag, a.dev_err)) goto mma_done;
-          if (!wait_bar<PAIR>(smem_u32(&bfull[sbi]), pb, abort_flag, a.dev_err)) goto mma_done;
-          if (rows_gathered) fence_proxy_async_smem();  // cp.async (generic proxy) rows -> tensor core
+          if (tg == 0) {
+            if (!wait_bar<PAIR>(smem_u32(&bfull[sbi]), pb, abort_flag, a.dev_err)) goto mma_done;
+            if (rows_gathered) fence_proxy_async_smem();  // cp.async (generic proxy) rows -> tensor core
+          }
           tc_fence_after();
           if (prev_sbi >= 0) {
-            commit_any<PAIR>(smem_u32(&bempty[prev_sbi]));
+            if (prev_rel_b) commit_any<PAIR>(smem_u32(&bempty[prev_sbi]));
             commit_any<PAIR>(smem_u32(&aempty[prev_sa]));
           }
           const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((sbi * Cfg::kBBytes) >> 4);
           const uint32_t a_tmem = tmem_base + Cfg::kACol0 + sa * (KS * 32);
-          const uint32_t acc0 = kb > un.kb0 ? 1u : 0u;
+          const uint32_t acc0 = bs > 0 ? 1u : 0u;
+          const uint32_t dt = d_tmem + static_cast<uint32_t>(tg * NT);
           if (nsub == KS) {
 #pragma unroll
             for (int sb = 0; sb < KS; ++sb) {
               const uint64_t bd = b_desc + static_cast<uint64_t>((sb * Cfg::kSubB) >> 4);
               const uint32_t at = a_tmem + sb * 32;
-              mma_any<PAIR>(d_tmem, at, bd, idesc, sb > 0 ? 1u : acc0);
-              mma_any<PAIR>(d_tmem, at + 8, bd + 2, idesc, 1u);
-              mma_any<PAIR>(d_tmem, at + 16, bd + 4, idesc, 1u);
-              mma_any<PAIR>(d_tmem, at + 24, bd + 6, idesc, 1u);
+              mma_any<PAIR>(dt, at, bd, idesc, sb > 0 ? 1u : acc0);
+              mma_any<PAIR>(dt, at + 8, bd + 2, idesc, 1u);
+              mma_any<PAIR>(dt, at + 16, bd + 4, idesc, 1u);
+              mma_any<PAIR>(dt, at + 24, bd + 6, idesc, 1u);
             }
           } else {  // K tail shorter than a full stage
             for (int sb = 0; sb < nsub; ++sb) {
               const uint64_t bd = b_desc + static_cast<uint64_t>((sb * Cfg::kSubB) >> 4);
               const uint32_t at = a_tmem + sb * 32;
-              mma_any<PAIR>(d_tmem, at, bd, idesc, sb > 0 ? 1u : acc0);
-              mma_any<PAIR>(d_tmem, at + 8, bd + 2, idesc, 1u);
-              mma_any<PAIR>(d_tmem, at + 16, bd + 4, idesc, 1u);
-              mma_any<PAIR>(d_tmem, at + 24, bd + 6, idesc, 1u);
+              mma_any<PAIR>(dt, at, bd, idesc, sb > 0 ? 1u : acc0);
+              mma_any<PAIR>(dt, at + 8, bd + 2, idesc, 1u);
+              mma_any<PAIR>(dt, at + 16, bd + 4, idesc, 1u);
+              mma_any<PAIR>(dt, at + 24, bd + 6, idesc, 1u);
             }
           }
           prev_sbi = sbi;
           prev_sa = sa;
+          prev_rel_b = tg == tpu - 1;
+          ++bs;
+          if (tpu > 1 && bs * KS >= a.n_kb) {  // next tile of the group
+            bs = 0;
+            ++tg;
+          }
         }
         if (prev_sbi >= 0) {
-          commit_any<PAIR>(smem_u32(&bempty[prev_sbi]));
+          if (prev_rel_b) commit_any<PAIR>(smem_u32(&bempty[prev_sbi]));
           commit_any<PAIR>(smem_u32(&aempty[prev_sa]));
         }
         commit_any<PAIR>(smem_u32(&accfull[ab]));
+        itb += static_cast<uint32_t>(tpu > 1 ? a.n_kb / KS : bs);
         ++lu;
       }
     mma_done:
@@ -726,10 +749,15 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       if (t == 0) red_release_add(a2.sync, 1);
     }
     // Plain calls on 64- and 128-token blocks without the SiLU epilogue (the FP32 down
-    // projection, whose epilogue bounds it at prefill) load the next unit's row ids while
-    // draining this one: measured on GB300, Qwen3 T=4096 down 116.7 -> 113 us; the SiLU
-    // epilogue and 16-token blocks ran 0.1-0.7 us slower with it.
-    const bool ids_ahead = !FUSED && !CL && NT >= 64 && a.epilogue != W4A16_EPILOGUE_SILU_MUL;
+    // projection, whose epilogue bounds it at prefill), and plain calls whose units are at
+    // most two pipeline stages (K <= 512), load the next unit's row ids while draining this
+    // one.  Measured on GB300: Qwen3 T=4096 down 116.7 -> 113 us; Kimi-K2 TP8 down (K = 256,
+    // 16-token blocks) 70.3 -> 64.2 us at T=32, 137.9 -> 125.6 at T=256, 193.2 -> 178.8 at
+    // T=1024 (single flushed calls); the SiLU epilogue and 16-token blocks of longer units
+    // ran 0.1-0.7 us slower with it.  (Loading every role's expert ids two units ahead was
+    // slower everywhere, e.g. the TP8 down at T=1024 back to 211.6 us.)
+    const bool ids_ahead = !FUSED && !CL &&
+                           ((NT >= 64 && a.epilogue != W4A16_EPILOGUE_SILU_MUL) || a.n_kb <= 8);
     int64_t ahead_u = -1;
     int32_t ahead_row = 0;
     for (int64_t u = CL ? unit0 : blockIdx.x; u < n_units; u += CL ? ustride : gridDim.x) {
@@ -757,29 +785,36 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
         sums_zeroed = true;
       }
       tc_fence_after();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ab * NT;
+      // a tile group's accumulators sit side by side: tpu * NT columns, tile c / NT
+      constexpr int ncol = NT * TPU;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ab * ncol;
       if (split_k == 1) {
         // TMEM loads are double-buffered: the next 16 columns are in flight while the current
         // ones are converted and stored.
+        auto store_cols = [&](int c, const uint32_t(&r)[16]) {
+          Unit ut = un;
+          ut.jt = un.jt + c / NT;
+          store_chunk16(g, ut, q, lane, c % NT, epi_rows, r, epi_stage);
+        };
         uint32_t r0[16], r1[16];
         tmem_ld16(taddr, r0);
 #pragma unroll 1
-        for (int c0 = 0; c0 < NT; c0 += 32) {
+        for (int c0 = 0; c0 < ncol; c0 += 32) {
           tmem_wait_ld16(r0);
-          if (c0 + 16 < NT) tmem_ld16(taddr + c0 + 16, r1);
-          if (c0 + 16 >= NT) {
+          if (c0 + 16 < ncol) tmem_ld16(taddr + c0 + 16, r1);
+          if (c0 + 16 >= ncol) {
             tc_fence_before();
             arrive_handoff<PAIR>(smem_u32(&accempty[ab]), leader, lane);
           }
-          store_chunk16(g, un, q, lane, c0, epi_rows, r0, epi_stage);
-          if (c0 + 16 < NT) {
+          store_cols(c0, r0);
+          if (c0 + 16 < ncol) {
             tmem_wait_ld16(r1);
-            if (c0 + 32 < NT) tmem_ld16(taddr + c0 + 32, r0);
-            if (c0 + 32 >= NT) {
+            if (c0 + 32 < ncol) tmem_ld16(taddr + c0 + 32, r0);
+            if (c0 + 32 >= ncol) {
               tc_fence_before();
               arrive_handoff<PAIR>(smem_u32(&accempty[ab]), leader, lane);
             }
-            store_chunk16(g, un, q, lane, c0 + 16, epi_rows, r1, epi_stage);
+            store_cols(c0 + 16, r1);
           }
         }
       } else {
@@ -866,13 +901,20 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
     for (int64_t u = CL ? unit0 : blockIdx.x; u < n_units; u += CL ? ustride : gridDim.x) {
       const Unit un = decode_any<FUSED, CL>(a, a2, split_k, units0_u, crank, u);
       if (!un.ok) continue;
-      // the tile's INT4 conversion (uniform over the unit, read while the weights are in flight)
+      // the tile's INT4 conversion (uniform over a tile, read while the weights are in flight;
+      // a tile group's modes are read together, one byte per tile)
       const GemmArgs& ga = args_of<FUSED>(a, a2, un);
-      const bool scaled =
-          __ldg(ga.tile_mode + static_cast<int64_t>(un.e) * ga.n_tiles + un.jt) == kTileScaled;
+      constexpr int tpu = TPU;
+      uint32_t modes = 0;
+      for (int j = 0; j < tpu; ++j)
+        modes |= static_cast<uint32_t>(
+                     __ldg(ga.tile_mode + static_cast<int64_t>(un.e) * ga.n_tiles + un.jt + j))
+                 << (8 * j);
       const bool nvfp4 = ga.nvfp4 != 0;
       for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
         if (it % kDqGroups != static_cast<uint32_t>(g)) continue;
+        const int tg = tpu > 1 ? kb / ga.n_kb : 0;  // tile of the group this stage belongs to
+        const bool scaled = ((modes >> (8 * tg)) & 0xFFu) == kTileScaled;
         const int nsub = min(KS, un.kb1 - kb);
         const int sw = it % S_W;
         const uint32_t pw = (it / S_W) & 1;
@@ -952,10 +994,10 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
   }
 }
 
-template <int NT, int KS>
+template <int NT, int KS, int TPU>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmArgs a) {
-  gemm_body<NT, KS, false>(a, a);
+  gemm_body<NT, KS, false, false, TPU>(a, a);
 }
 
 // CTA pairs (128-token blocks): launched as two-CTA clusters; one M = 256 MMA covers the two
@@ -1062,13 +1104,13 @@ cudaError_t make_act_tmap(CUtensorMap* map, const uint16_t* A, int64_t rows, int
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int NT>
-cudaError_t launch_gemm_t(GemmArgs& args, int grid, bool pdl, cudaStream_t stream) {
+template <int NT, int TPU>
+cudaError_t launch_gemm_tpu(GemmArgs& args, int grid, bool pdl, cudaStream_t stream) {
   constexpr int KS = StageK<NT>::value;
-  using Cfg = GemmCfg<NT, KS>;
+  using Cfg = GemmCfg<NT, KS, false, TPU>;
   static bool configured = false;  // per-process; attribute applies to the current device
   if (!configured) {
-    cudaError_t err = cudaFuncSetAttribute(moe_gemm_kernel<NT, KS>,
+    cudaError_t err = cudaFuncSetAttribute(moe_gemm_kernel<NT, KS, TPU>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(Cfg::kSmemBytes));
     if (err != cudaSuccess) return err;
@@ -1084,7 +1126,17 @@ cudaError_t launch_gemm_t(GemmArgs& args, int grid, bool pdl, cudaStream_t strea
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, moe_gemm_kernel<NT, KS>, args);
+  return cudaLaunchKernelEx(&cfg, moe_gemm_kernel<NT, KS, TPU>, args);
+}
+
+template <int NT>
+cudaError_t launch_gemm_t(GemmArgs& args, int grid, bool pdl, cudaStream_t stream) {
+  if constexpr (tile_group_max(NT) >= 4)
+    if (args.tpu == 4) return launch_gemm_tpu<NT, 4>(args, grid, pdl, stream);
+  if constexpr (tile_group_max(NT) >= 2)
+    if (args.tpu == 2) return launch_gemm_tpu<NT, 2>(args, grid, pdl, stream);
+  if (args.tpu != 1) return cudaErrorInvalidValue;
+  return launch_gemm_tpu<NT, 1>(args, grid, pdl, stream);
 }
 
 template <int NT>

@@ -15,7 +15,10 @@ struct GemmArgs {
   int a_sorted;
   const uint8_t* wblob;
   int E, N, K, n_tiles, n_kb;
-  uint32_t nt_magic, nt_shift;  // division by n_tiles: (umulhi(n, magic) + n) >> shift
+  // Tile groups (short-K plain calls): a unit covers tpu consecutive 128-row tiles of one
+  // block, n_tg = n_tiles / tpu units per block (tpu = 1: one tile per unit)
+  int tpu, n_tg;
+  uint32_t nt_magic, nt_shift;  // division by n_tg: (umulhi(n, magic) + n) >> shift
   int paired;
   int nvfp4;  // the blob holds NVFP4 (E2M1 + E4M3 per 16) weights instead of INT4
   const uint8_t* tile_mode;  // [E * n_tiles] kTilePlain / kTileScaled (INT4 conversion of a tile)
@@ -68,6 +71,12 @@ struct GemmArgs {
 constexpr int kMinSplitKb = 24;
 // Most K slices the planner lets the device choose.
 constexpr int kMaxAutoSplit = 8;
+
+// Largest tile group for a block size: its double-buffered accumulators (2 * tpu * block_m
+// TMEM columns) stay within the 128 columns reserved for them below 64-token blocks.
+constexpr int tile_group_max(int block_m) { return block_m <= 16 ? 4 : (block_m <= 32 ? 2 : 1); }
+// K blocks (64 wide) of a unit short enough for tile groups: at most two pipeline stages.
+constexpr int kGroupMaxKb = 8;
 
 // The fused layer call: gate_up (a) then down (a2) in one cooperative persistent launch.
 cudaError_t launch_layer_fused(GemmArgs& a, GemmArgs& a2, int grid, cudaStream_t stream);
