@@ -369,3 +369,27 @@ def test_layer_kimi_sampled_tokens(lib, name, T):
     assert_close_bf16(out[sub], ref, f"{name} T={T}")
     none_local = (inp.topk_ids < 0).all(dim=1)
     assert torch.all(out[none_local].float() == 0)
+
+
+@pytest.mark.parametrize("bm,split", [(16, 1), (32, 1), (64, 1), (128, 1), (16, 3), (128, 2)])
+def test_gemm_fp32_sorted_rows_equal_slot_rows(lib, bm, split):
+    # FP32 sums in sorted rows: the same values, bit for bit, as FP32 rows by slot; padding
+    # positions are zeros, rows past the last block untouched
+    T, k, E, N, K = 90, 4, 9, 768, 512
+    qw, sc, x, ids, W, r, (s, e, ntp) = _gemm_case(lib, T, k, E, N, K, bm, 71)
+    xs = lib.gather_rows(x.to(DEV), k, r)
+    flags = lib.A_ROWS_SORTED | lib.C_FP32
+    by_slot = lib.moe_gemm(xs, 1, W, r, row_flags=flags, split_k=split).cpu()
+    out = torch.full((r.capacity, N), float("nan"), dtype=torch.float32, device=DEV)
+    lib.moe_gemm(xs, 1, W, r, row_flags=flags | lib.C_ROWS_SORTED, out=out, split_k=split)
+    got = out.cpu()
+    for p in range(ntp):
+        i = int(s[p])
+        if i < T * k:
+            assert torch.equal(got[p].view(torch.int32), by_slot[i].view(torch.int32)), p
+        else:
+            assert torch.all(got[p] == 0), p
+    assert torch.isnan(got[ntp:]).all()
+    ref = oracle.moe_gemm(x, k, qw, sc, s, e, ntp, bm, T * k, out_f32=True)
+    rows = routed_rows(ids)
+    assert_close_bf16(by_slot[rows], ref[rows], f"FP32 rows bm={bm} split={split}")

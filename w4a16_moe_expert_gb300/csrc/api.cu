@@ -377,8 +377,10 @@ static w4a16_status_t prepare_gemm(const GemmCall& c, const DeviceFacts& dev, Ge
                   want_group, want_group == 2 ? 32 : 16);
     tpu = want_group;
   } else if (want_group == 0 && group_ok) {
+    // the largest group that divides the tiles and still leaves a unit for every CTA (by the
+    // planner's estimate of routed blocks): at T=1 parallelism matters more than amortising
     tpu = group_max;
-    while (tpu > 1 && a.n_tiles % tpu) tpu >>= 1;
+    while (tpu > 1 && (a.n_tiles % tpu || static_cast<int64_t>(plan.est_units) / tpu < grid)) tpu >>= 1;
   }
   if (tpu > 1) {
     a.tpu = tpu;
