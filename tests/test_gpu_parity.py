@@ -393,3 +393,46 @@ def test_gemm_fp32_sorted_rows_equal_slot_rows(lib, bm, split):
     ref = oracle.moe_gemm(x, k, qw, sc, s, e, ntp, bm, T * k, out_f32=True)
     rows = routed_rows(ids)
     assert_close_bf16(by_slot[rows], ref[rows], f"FP32 rows bm={bm} split={split}")
+
+
+@pytest.mark.parametrize("epilogue,flags", [(0, 0), (1, 0), (0, 4)])
+def test_gemm_last_partial_wave_sliced(lib, epilogue, flags):
+    # 4 blocks x 12 tiles = 48 units on 40 CTAs: one full wave of whole tiles, then the last 8
+    # tiles cut into K slices (4 of 24 K blocks each, summed in slice order by the tile's last
+    # CTA) so the partial wave fills the grid.  Checked against the oracle; two calls are
+    # bitwise equal, and the tiles of the full wave equal the unsliced schedule bit for bit.
+    T, k, E, N, K = 8, 4, 4, 1536, 6144
+    qw, sc, x, ids, W, r, (s, e, ntp) = _gemm_case(lib, T, k, E, N, K, 16, 81, paired=bool(epilogue))
+    assert ntp // 16 == 4
+    kw = dict(epilogue=epilogue, row_flags=flags, num_ctas=40)
+    a = lib.moe_gemm(x.to(DEV), k, W, r, **kw).cpu()
+    b = lib.moe_gemm(x.to(DEV), k, W, r, **kw).cpu()
+    whole = lib.moe_gemm(x.to(DEV), k, W, r, split_k=1, **kw).cpu()
+    f32 = bool(flags & lib.C_FP32)
+    view = (lambda t: t.view(torch.int32)) if f32 else bits
+    assert torch.equal(view(a), view(b))
+    ref = oracle.moe_gemm(x, k, qw, sc, s, e, ntp, 16, T * k, out_f32=bool(epilogue) or f32,
+                          threads=4)
+    if epilogue:
+        ref = oracle.silu_mul(ref)
+    rows = routed_rows(ids)
+    assert_close_bf16(a[rows], ref[rows], "sliced last wave")
+    # the sliced tiles really were summed in a different order somewhere
+    assert not torch.equal(view(a), view(whole))
+    # units 0..39 are whole tiles: blocks 0..2 (tiles 0..35) and block 3's tiles 0..3
+    tile_cols = 64 if epilogue else 128
+    first_tiles = 4  # of block 3
+    for p in range(ntp):
+        i = int(s[p])
+        if i >= T * k:
+            continue
+        blk = p // 16
+        if blk < 3:
+            assert torch.equal(view(a[i]), view(whole[i])), (p, i)
+        else:
+            if epilogue:
+                # paired SiLU output: tile j writes columns 64j .. 64j + 63
+                cols = slice(0, first_tiles * tile_cols)
+            else:
+                cols = slice(0, first_tiles * tile_cols)
+            assert torch.equal(view(a[i, cols]), view(whole[i, cols])), (p, i)

@@ -36,8 +36,8 @@ def test_groups_match_oracle_and_one_tile_per_unit(lib, bm, group, K):
     # gathered activation rows (a_row_div = top_k), BF16 output by slot
     T, k, E, N = 40, 4, 12, 1024
     qw, sc, x, ids, W, r, (s, e, ntp) = _case(lib, T, k, E, N, K, bm, 61 + K)
-    one = lib.moe_gemm(x.to(DEV), k, W, r, tile_group=1).cpu()
-    grp = lib.moe_gemm(x.to(DEV), k, W, r, tile_group=group).cpu()
+    one = lib.moe_gemm(x.to(DEV), k, W, r, tile_group=1, split_k=1).cpu()  # whole K, one tile
+    grp = lib.moe_gemm(x.to(DEV), k, W, r, tile_group=group, split_k=1).cpu()
     ref = oracle.moe_gemm(x, k, qw, sc, s, e, ntp, bm, T * k)
     rows = routed_rows(ids)
     assert_close_bf16(grp[rows], ref[rows], f"tile group {group}, bm {bm}, K {K}")
@@ -51,8 +51,8 @@ def test_groups_down_projection_layout_fp32(lib, bm):
     qw, sc, x, ids, W, r, (s, e, ntp) = _case(lib, T, k, E, N, K, bm, 62)
     h = lib.gather_rows(x.to(DEV), k, r)
     flags = lib.A_ROWS_SORTED | lib.C_FP32
-    one = lib.moe_gemm(h, 1, W, r, row_flags=flags, tile_group=1).cpu()
-    grp = lib.moe_gemm(h, 1, W, r, row_flags=flags).cpu()  # planner: the largest group
+    one = lib.moe_gemm(h, 1, W, r, row_flags=flags, tile_group=1, split_k=1).cpu()
+    grp = lib.moe_gemm(h, 1, W, r, row_flags=flags, split_k=1).cpu()  # planner's group
     assert torch.equal(one.view(torch.int32), grp.view(torch.int32))
     ref = oracle.moe_gemm(x, k, qw, sc, s, e, ntp, bm, T * k, out_f32=True)
     rows = routed_rows(ids)
@@ -63,7 +63,7 @@ def test_groups_with_silu_epilogue_and_sorted_output(lib):
     T, k, E, N, K = 30, 2, 10, 1024, 256
     qw, sc, x, ids, W, r, (s, e, ntp) = _case(lib, T, k, E, N, K, 16, 63, paired=True)
     kw = dict(epilogue=lib.EPILOGUE_SILU_MUL, row_flags=lib.C_ROWS_SORTED)
-    one = lib.moe_gemm(x.to(DEV), k, W, r, tile_group=1, **kw).cpu()
+    one = lib.moe_gemm(x.to(DEV), k, W, r, tile_group=1, split_k=1, **kw).cpu()
     grp = lib.moe_gemm(x.to(DEV), k, W, r, tile_group=4, **kw).cpu()
     assert torch.equal(bits(one[:ntp]), bits(grp[:ntp]))
     ref = oracle.silu_mul(oracle.moe_gemm(x, k, qw, sc, s, e, ntp, 16, T * k, out_f32=True))
@@ -78,8 +78,8 @@ def test_tile_count_not_a_multiple_falls_back_and_bad_groups_are_rejected(lib):
     # blocks, not whole stages) and K = 1024 (four stages) are never grouped
     T, k, E = 20, 2, 6
     qw, sc, x, ids, W, r, (s, e, ntp) = _case(lib, T, k, E, 384, 256, 16, 64)
-    a = lib.moe_gemm(x.to(DEV), k, W, r).cpu()
-    b = lib.moe_gemm(x.to(DEV), k, W, r, tile_group=1).cpu()
+    a = lib.moe_gemm(x.to(DEV), k, W, r, split_k=1).cpu()
+    b = lib.moe_gemm(x.to(DEV), k, W, r, tile_group=1, split_k=1).cpu()
     assert torch.equal(bits(a), bits(b))
     with pytest.raises(lib.LibraryError):
         lib.moe_gemm(x.to(DEV), k, W, r, tile_group=2)

@@ -364,8 +364,10 @@ static w4a16_status_t prepare_gemm(const GemmCall& c, const DeviceFacts& dev, Ge
   // activation stages and its per-unit hand-offs.
   const int group_max = tile_group_max(R->block_m);
   const int stage_kb = R->block_m <= 64 ? 4 : 2;
-  const bool group_ok = !a.pair && !c.merge_w && !c.one_kernel && a.split_k == 1 &&
-                        !a.split_auto && n_kb <= kGroupMaxKb && n_kb % stage_kb == 0;
+  // (a planner's split of short K yields to the group; a fixed split excludes it)
+  const bool group_ok = !a.pair && !c.merge_w && !c.one_kernel &&
+                        (a.split_k == 1 || a.split_auto) && n_kb <= kGroupMaxKb &&
+                        n_kb % stage_kb == 0;
   const int want_group = c.sched ? c.sched->tile_group : 0;
   if (want_group < 0 || want_group > 4 || want_group == 3)
     return fail(W4A16_INVALID_ARG, "tile_group %d: supported values are 0, 1, 2, 4", want_group);
@@ -383,6 +385,8 @@ static w4a16_status_t prepare_gemm(const GemmCall& c, const DeviceFacts& dev, Ge
     while (tpu > 1 && (a.n_tiles % tpu || static_cast<int64_t>(plan.est_units) / tpu < grid)) tpu >>= 1;
   }
   if (tpu > 1) {
+    a.split_k = 1;
+    a.split_auto = 0;
     a.tpu = tpu;
     a.n_tg = a.n_tiles / tpu;
     fast_divisor(static_cast<uint32_t>(a.n_tg), &a.nt_magic, &a.nt_shift);

@@ -81,29 +81,50 @@ struct GemmCfg {
 
 struct Unit {
   int b, jt, split, kb0, kb1, e;
-  int gi;  // which GEMM of a fused layer call (0: gate_up, 1: down); 0 otherwise
+  int gi;      // which GEMM of a fused layer call (0: gate_up, 1: down); 0 otherwise
+  int nsplit;  // K slices of this unit's tile (1: whole K)
+  int ptile;   // index of a sliced tile among the sliced tiles (partial sums, counters)
   int64_t tile;
   bool ok;  // the block names a valid expert
 };
 
-// Unit u -> (block, tile, split).  Every role decodes every unit, so the divisions are 32-bit
-// (the host keeps unit counts below 2^31) and the one by n_tiles uses a precomputed
-// multiply-shift: q = (umulhi(n, m) + n) >> s with m = ceil(2^(32+s) / d) - 2^32 and
-// s = ceil(log2 d), exact for n < 2^31 (round-up reciprocal method).
-__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int split_k, int64_t u64) {
+// Which units are K slices: units [0, tail) are whole tiles 0 .. tail-1; the units from tail
+// on are the remaining tiles, each cut into s K slices (unit tail + p*s + j: slice j of tile
+// tail + p).  No slicing: tail past the last unit.
+struct SplitMap {
+  uint32_t tail;
+  uint32_t s;
+};
+__device__ __forceinline__ SplitMap no_split() { return SplitMap{0xFFFFFFFFu, 1u}; }
+
+// Unit u -> (block, tile, slice).  Every role decodes every unit, so the divisions are 32-bit
+// (the host keeps unit counts below 2^31) and the one by the tiles per block uses a
+// precomputed multiply-shift: q = (umulhi(n, m) + n) >> s with m = ceil(2^(32+s) / d) - 2^32
+// and s = ceil(log2 d), exact for n < 2^31 (round-up reciprocal method).
+__device__ __forceinline__ uint32_t unit_tile(const SplitMap& sm, uint32_t u) {
+  return u < sm.tail ? u : sm.tail + (u - sm.tail) / sm.s;
+}
+
+__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, const SplitMap& sm, int64_t u64) {
   const uint32_t u = static_cast<uint32_t>(u64);
   Unit t;
   uint32_t tile;
-  if (split_k == 1) {
+  if (u < sm.tail) {
     tile = u;
     t.split = 0;
+    t.nsplit = 1;
+    t.ptile = 0;
     t.kb0 = 0;
     t.kb1 = a.n_kb * a.tpu;  // a tile group's tiles are consecutive chunks of one strip
   } else {
-    tile = u / static_cast<uint32_t>(split_k);
-    t.split = static_cast<int>(u - tile * static_cast<uint32_t>(split_k));
-    t.kb0 = t.split * a.n_kb / split_k;
-    t.kb1 = (t.split + 1) * a.n_kb / split_k;
+    const uint32_t v = u - sm.tail;
+    const uint32_t pt = v / sm.s;
+    t.split = static_cast<int>(v - pt * sm.s);
+    t.nsplit = static_cast<int>(sm.s);
+    t.ptile = static_cast<int>(pt);
+    tile = sm.tail + pt;
+    t.kb0 = t.split * a.n_kb / t.nsplit;
+    t.kb1 = (t.split + 1) * a.n_kb / t.nsplit;
   }
   const uint32_t b = (__umulhi(tile, a.nt_magic) + tile) >> a.nt_shift;
   t.tile = tile;
@@ -116,9 +137,8 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int split_k, int6
 }
 
 // The aligned block of unit u (plain calls): the block part of decode_unit, without the loads.
-__device__ __forceinline__ uint32_t unit_block(const GemmArgs& a, int split_k, int64_t u64) {
-  const uint32_t u = static_cast<uint32_t>(u64);
-  const uint32_t tile = split_k == 1 ? u : u / static_cast<uint32_t>(split_k);
+__device__ __forceinline__ uint32_t unit_block(const GemmArgs& a, const SplitMap& sm, int64_t u64) {
+  const uint32_t tile = unit_tile(sm, static_cast<uint32_t>(u64));
   return (__umulhi(tile, a.nt_magic) + tile) >> a.nt_shift;
 }
 
@@ -132,6 +152,8 @@ __device__ __forceinline__ Unit decode_unit_pair(const GemmArgs& a, uint32_t cra
   t.b = static_cast<int>(b);
   t.jt = static_cast<int>(2 * (u - b * static_cast<uint32_t>(a.n_tiles >> 1)) + crank);
   t.split = 0;
+  t.nsplit = 1;
+  t.ptile = 0;
   t.kb0 = 0;
   t.kb1 = a.n_kb;
   t.gi = 0;
@@ -143,13 +165,14 @@ __device__ __forceinline__ Unit decode_unit_pair(const GemmArgs& a, uint32_t cra
 // Fused layer: units [0, units0) are the first GEMM's (gate_up), the rest the second's (down),
 // both over the same aligned blocks.  A plain call has one GEMM (a2 is a).
 template <bool FUSED, bool PAIR = false>
-__device__ __forceinline__ Unit decode_any(const GemmArgs& a, const GemmArgs& a2, int split_k,
-                                           uint32_t units0, uint32_t crank, int64_t u64) {
+__device__ __forceinline__ Unit decode_any(const GemmArgs& a, const GemmArgs& a2,
+                                           const SplitMap& sm, uint32_t units0, uint32_t crank,
+                                           int64_t u64) {
   if (PAIR) return decode_unit_pair(a, crank, u64);
-  if (!FUSED) return decode_unit(a, split_k, u64);
+  if (!FUSED) return decode_unit(a, sm, u64);
   const uint32_t u = static_cast<uint32_t>(u64);
-  if (u < units0) return decode_unit(a, 1, u);
-  Unit t = decode_unit(a2, 1, u - units0);
+  if (u < units0) return decode_unit(a, no_split(), u);
+  Unit t = decode_unit(a2, no_split(), u - units0);
   t.gi = 1;
   return t;
 }
@@ -433,21 +456,43 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
   if (ntp < 0) ntp = 0;
   if (ntp > a.capacity) ntp = static_cast<int>(a.capacity);
   const int64_t nblocks = ntp / a.block_m;
-  // Decode schedule from the routed blocks: when the (block, tile) units leave SMs idle, each
-  // tile's K range is sliced so that the units fill one wave (every role computes the same
-  // count from num_tokens_padded).  Fewer K splits when the routed blocks would overflow the
-  // partial-sum scratch.
-  int split_k = a.split_k;
-  if (a.split_auto) {
-    const int64_t units1 = nblocks * a.n_tg;
-    int s = units1 > 0 ? static_cast<int>(min(static_cast<int64_t>(split_k),
-                                              static_cast<int64_t>(gridDim.x) / units1))
-                       : 1;
-    while (s > 1 && a.n_kb < s * kMinSplitKb) --s;
-    split_k = s > 1 ? s : 1;
+  // Decode schedule from the routed blocks (every role computes the same map from
+  // num_tokens_padded).  When the whole-tile units end in a partial wave of at most half the
+  // grid, the tiles of that last wave are cut into K slices (of >= kMinSplitKb K blocks) that
+  // fill it: with no full wave (few tiles, long K) every tile is sliced.  A fixed split slices
+  // every tile.  Fewer slices when the sliced tiles would overflow the partial-sum scratch.
+  const int64_t units1 = nblocks * a.n_tg;
+  SplitMap sm = no_split();
+  int64_t units_split = units1;
+  if (!FUSED && !CL && units1 > 0) {
+    int64_t tail = units1;
+    int sn = 1;
+    if (a.split_auto) {
+      const int64_t G = gridDim.x;
+      const int64_t R = units1 % G;
+      if (R > 0 && 2 * R <= G) {
+        int ss = static_cast<int>(min(static_cast<int64_t>(a.split_k), G / R));
+        while (ss > 1 && (a.n_kb < ss * kMinSplitKb || R * ss > a.max_split_units)) --ss;
+        if (ss > 1) {
+          sn = ss;
+          tail = units1 - R;
+        }
+      }
+    } else if (a.split_k > 1) {
+      int ss = a.split_k;
+      while (ss > 1 && units1 * ss > a.max_split_units) --ss;
+      if (ss > 1) {
+        sn = ss;
+        tail = 0;
+      }
+    }
+    if (sn > 1) {
+      sm.tail = static_cast<uint32_t>(tail);
+      sm.s = static_cast<uint32_t>(sn);
+      units_split = tail + (units1 - tail) * sn;
+    }
   }
-  while (split_k > 1 && nblocks * a.n_tg * split_k > a.max_split_units) --split_k;
-  const int64_t units0 = CL ? nblocks * (a.n_tiles >> 1) : nblocks * a.n_tg * split_k;
+  const int64_t units0 = CL ? nblocks * (a.n_tiles >> 1) : units_split;
   const int64_t n_units = FUSED ? units0 + nblocks * a2.n_tg : units0;
   const uint32_t units0_u = static_cast<uint32_t>(units0);
 
@@ -459,7 +504,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
     const uint64_t policy = a.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
     uint32_t it = 0;
     for (int64_t u = CL ? unit0 : blockIdx.x; u < n_units; u += CL ? ustride : gridDim.x) {
-      const Unit un = decode_any<FUSED, CL>(a, a2, split_k, units0_u, crank, u);
+      const Unit un = decode_any<FUSED, CL>(a, a2, sm, units0_u, crank, u);
       if (!un.ok) continue;
       const GemmArgs& g = args_of<FUSED>(a, a2, un);
       const uint8_t* strip = g.wblob + kHeaderBytes +
@@ -494,7 +539,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       const int c = gt & 7;
       constexpr int R = NT / 8;
       for (int64_t u = CL ? unit0 : blockIdx.x; u < n_units; u += CL ? ustride : gridDim.x) {
-        const Unit un = decode_any<FUSED, CL>(a, a2, split_k, units0_u, crank, u);
+        const Unit un = decode_any<FUSED, CL>(a, a2, sm, units0_u, crank, u);
         if (!un.ok) continue;
         const GemmArgs& g = args_of<FUSED>(a, a2, un);
         if (g.wait_done) {
@@ -561,7 +606,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       const int c = g & 7;  // 16-byte chunk of a 128-byte row handled by this thread
       constexpr int R = NT / 8;  // rows per thread: (g >> 3) + 8j
       for (int64_t u = CL ? unit0 : blockIdx.x; u < n_units; u += CL ? ustride : gridDim.x) {
-        const Unit un = decode_any<FUSED, CL>(a, a2, split_k, units0_u, crank, u);
+        const Unit un = decode_any<FUSED, CL>(a, a2, sm, units0_u, crank, u);
         if (!un.ok) continue;
         int32_t arow[R];
 #pragma unroll
@@ -596,7 +641,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
     } else if (warp == 2) {
       // rows already in sorted order: one 2-D TMA tile per K sub-block, rotating lanes
       for (int64_t u = CL ? unit0 : blockIdx.x; u < n_units; u += CL ? ustride : gridDim.x) {
-        const Unit un = decode_any<FUSED, CL>(a, a2, split_k, units0_u, crank, u);
+        const Unit un = decode_any<FUSED, CL>(a, a2, sm, units0_u, crank, u);
         if (!un.ok) continue;
         const int kb_end = TPU > 1 ? a.n_kb : un.kb1;  // tile groups: loaded once
         for (int kb = un.kb0; kb < kb_end; kb += KS, ++it) {
@@ -633,7 +678,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       if (elect_one()) {
         uint32_t it = 0;
         for (int64_t u = CL ? unit0 : blockIdx.x; u < n_units; u += CL ? ustride : gridDim.x) {
-          const Unit un = decode_any<FUSED, CL>(a, a2, split_k, units0_u, crank, u);
+          const Unit un = decode_any<FUSED, CL>(a, a2, sm, units0_u, crank, u);
           if (!un.ok) continue;
           for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
             const int sbi = it % S_B;
@@ -649,7 +694,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       uint32_t it = 0, itb = 0, lu = 0;  // A ring, activation ring, accumulator positions
       constexpr int tpu = TPU;
       for (int64_t u = CL ? unit0 : blockIdx.x; u < n_units; u += CL ? ustride : gridDim.x) {
-        const Unit un = decode_any<FUSED, CL>(a, a2, split_k, units0_u, crank, u);
+        const Unit un = decode_any<FUSED, CL>(a, a2, sm, units0_u, crank, u);
         if (!un.ok) continue;
         const bool rows_gathered = FUSED ? !args_of<FUSED>(a, a2, un).a_sorted : gather;
         const int ab = lu & 1;
@@ -761,7 +806,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
     int64_t ahead_u = -1;
     int32_t ahead_row = 0;
     for (int64_t u = CL ? unit0 : blockIdx.x; u < n_units; u += CL ? ustride : gridDim.x) {
-      const Unit un = decode_any<FUSED, CL>(a, a2, split_k, units0_u, crank, u);
+      const Unit un = decode_any<FUSED, CL>(a, a2, sm, units0_u, crank, u);
       if (!un.ok) continue;
       const GemmArgs& g = args_of<FUSED>(a, a2, un);
       named_bar_epi();  // the previous unit's readers of epi_rows / last_flag are done
@@ -775,7 +820,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       if (epi_any(!ok)) break;
       if (ids_ahead && u + gridDim.x < n_units) {
         ahead_u = u + gridDim.x;
-        const uint32_t nb = unit_block(a, split_k, ahead_u);
+        const uint32_t nb = unit_block(a, sm, ahead_u);
         ahead_row = t < NT ? __ldg(a.sorted_ids + static_cast<int64_t>(nb) * a.block_m + t) : 0;
       }
       if (FUSED && g.sync && !sums_zeroed) {
@@ -788,7 +833,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       // a tile group's accumulators sit side by side: tpu * NT columns, tile c / NT
       constexpr int ncol = NT * TPU;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ab * ncol;
-      if (split_k == 1) {
+      if (un.nsplit == 1) {
         // TMEM loads are double-buffered: the next 16 columns are in flight while the current
         // ones are converted and stored.
         auto store_cols = [&](int c, const uint32_t(&r)[16]) {
@@ -818,7 +863,8 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
           }
         }
       } else {
-        float* part = a.part + (un.tile * split_k + un.split) * (128 * NT);
+        const int nsplit = un.nsplit;
+        float* part = a.part + (static_cast<int64_t>(un.ptile) * nsplit + un.split) * (128 * NT);
 #pragma unroll 1
         for (int c0 = 0; c0 < NT; c0 += 16) {
           uint32_t r[16];
@@ -833,18 +879,18 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
         }
         __threadfence();
         named_bar_epi();
-        if (t == 0) *last_flag = (atomicAdd(a.cnt + un.tile, 1) == split_k - 1) ? 1 : 0;
+        if (t == 0) *last_flag = (atomicAdd(a.cnt + un.ptile, 1) == nsplit - 1) ? 1 : 0;
         named_bar_epi();
         if (*last_flag) {
           __threadfence();
-          const float* tile_parts = a.part + un.tile * split_k * (128 * NT);
+          const float* tile_parts = a.part + static_cast<int64_t>(un.ptile) * nsplit * (128 * NT);
 #pragma unroll 1
           for (int c0 = 0; c0 < NT; c0 += 16) {
             // splits summed in order; the 16 columns of one split load together
             float v[16];
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) v[jj] = __ldcg(tile_parts + (c0 + jj) * 128 + t);
-            for (int s = 1; s < split_k; ++s) {
+            for (int s = 1; s < nsplit; ++s) {
               float w[16];
 #pragma unroll
               for (int jj = 0; jj < 16; ++jj)
@@ -857,7 +903,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
             for (int jj = 0; jj < 16; ++jj) r[jj] = __float_as_uint(v[jj]);
             store_chunk16(g, un, q, lane, c0, epi_rows, r, epi_stage);
           }
-          if (t == 0) a.cnt[un.tile] = 0;  // ready for the next call
+          if (t == 0) a.cnt[un.ptile] = 0;  // ready for the next call
         }
       }
       if (FUSED && g.signal_done) {
@@ -899,7 +945,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + Cfg::kACol0;
     uint32_t it = 0;
     for (int64_t u = CL ? unit0 : blockIdx.x; u < n_units; u += CL ? ustride : gridDim.x) {
-      const Unit un = decode_any<FUSED, CL>(a, a2, split_k, units0_u, crank, u);
+      const Unit un = decode_any<FUSED, CL>(a, a2, sm, units0_u, crank, u);
       if (!un.ok) continue;
       // the tile's INT4 conversion (uniform over a tile, read while the weights are in flight;
       // a tile group's modes are read together, one byte per tile)
@@ -1049,22 +1095,31 @@ double expected_blocks(int total_slots, int E, int block_m, double rows_per_expe
 }
 
 // Split-K: the split itself is chosen on the device from the routed block count (the host
-// cannot know it without a read-back).  The planner allows it where a slice keeps at least
-// kMinSplitKb K blocks and then launches one CTA per SM, so that a call whose routed units
-// leave SMs idle (one or a few experts with long K at decode, e.g. 32 tiles of K = 7168) can
-// slice K until the units fill the grid.  Where the units fill the grid no split happens:
-// measured on GB300, a second wave of half-length units plus the partial round trip is
-// slower than one wave of whole ones (Qwen3 T=1 gate_up, 96 units: 7.9 -> 11.1 us).
+// cannot know it without a read-back).  For decode block sizes the planner allows up to
+// kMaxAutoSplit slices of at least kMinSplitKb K blocks and launches one CTA per SM unless its
+// estimate of units fills half the grid without slicing.  On the device: where the routed
+// units leave SMs idle (one or a few experts with long K, e.g. 32 tiles of K = 7168) every
+// tile is sliced until the units fill one wave; where the units end in a partial wave of at
+// most half the grid, only that wave's tiles are sliced to fill it (Kimi-K2 EP8 T=16 gate_up,
+// 512 units on 152 CTAs: the last 56 tiles in two slices, 62.1 -> 58.0 us).
+// Measured on GB300: slicing K = 2048 in two with no full wave (Kimi-K2 EP8 down at T=1, 56
+// tiles -> 112 units) is slower (7.5 -> 8.3 us), slicing K = 7168 in four (32 tiles -> 128
+// units) much faster (gate_up 16.3 -> 10.5 us); a second wave of half-length units plus the
+// partial round trip is slower than one wave of whole ones (Qwen3 T=1 gate_up, 96 units:
+// 7.9 -> 11.1 us).
 void plan_gemm(int total_slots, int E, int N, int K, int block_m, int rows_per_expert,
                int num_sms, w4a16_plan_t* plan) {
   const int n_tiles = N / kTileRows, n_kb = K / kBlockK;
   const double blocks = expected_blocks(total_slots, E, block_m, rows_per_expert);
   const double units1 = std::max(1.0, std::ceil(blocks)) * n_tiles;
-  const int split_max = std::max(1, std::min(kMaxAutoSplit, n_kb / kMinSplitKb));
+  const int split_max =
+      block_m <= kMaxSplitBlockM ? std::max(1, std::min(kMaxAutoSplit, n_kb / kMinSplitKb)) : 1;
   plan->block_m = block_m;
   plan->split_k = split_max;
   plan->est_units = static_cast<int32_t>(std::min(units1, 2.0e9));
-  plan->num_ctas = split_max > 1 ? num_sms : std::max(1, std::min(num_sms, plan->est_units));
+  const bool few = 2.0 * units1 < num_sms;
+  plan->num_ctas = (split_max > 1 && few) ? num_sms
+                                          : std::max(1, std::min(num_sms, plan->est_units));
   plan->stages = stages_for_block_m(block_m);
 }
 

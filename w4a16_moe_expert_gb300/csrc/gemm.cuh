@@ -39,8 +39,9 @@ struct GemmArgs {
   float* part;
   int32_t* cnt;
   int split_k;
-  // split_k is an upper bound: the device takes as many K slices as keep the routed
-  // (block, tile) units within one wave of the grid, each slice at least kMinSplitKb K blocks
+  // split_k is an upper bound: the device slices the tiles of a last, partial wave of the
+  // routed (block, tile) units into K slices that fill it (every tile when there is no full
+  // wave), each slice at least kMinSplitKb K blocks
   int split_auto;
   int64_t max_split_units;  // K splits are reduced on the device until units fit the scratch
   int32_t* dev_err;
@@ -67,8 +68,14 @@ struct GemmArgs {
 // Fewest 64-wide K blocks one K slice of an automatically split tile streams (1536 K elements:
 // six pipeline stages at decode block sizes).  Measured on GB300: slicing K = 2048 in two
 // (Kimi-K2 EP8 down at T=1, 56 tiles -> 112 units) is slower (7.5 -> 8.3 us), slicing
-// K = 7168 in four (32 tiles -> 128 units) much faster (gate_up 16.3 -> 10.5 us).
+// K = 7168 in four (32 tiles -> 128 units) much faster (gate_up 16.3 -> 10.5 us); slicing the
+// last partial wave's tiles into slices of 4 K blocks was no faster at Qwen3 T=8 (K = 2048)
+// and slower at T=512 (64.2 -> 72.3 us gate_up).
 constexpr int kMinSplitKb = 24;
+// Largest block size whose calls the device may split (decode): at prefill the partial sums
+// of 128 x block_m tiles cost more than the last wave's imbalance (Qwen3 T=4096 down 117 ->
+// 126 us with the last wave sliced).
+constexpr int kMaxSplitBlockM = 32;
 // Most K slices the planner lets the device choose.
 constexpr int kMaxAutoSplit = 8;
 
