@@ -41,6 +41,13 @@ ALIGN_CASES = [
     (16384, 8, 384, 48, 128, "zipf"),
     (8192, 8, 384, 384, 128, "zipf"),
     (1000, 6, 1024, 1024, 16, "softmax"),
+    # decode routings of at most 32 slots (sorted by one warp in registers)
+    (2, 8, 128, 128, 16, "softmax"),
+    (3, 8, 128, 128, 32, "softmax"),
+    (4, 8, 128, 128, 64, "softmax"),
+    (4, 8, 16, 16, 128, "softmax"),
+    (4, 8, 384, 48, 16, "zipf"),
+    (31, 1, 4, 4, 16, "softmax"),
 ]
 
 
@@ -68,6 +75,28 @@ def test_align_validation_flags_bad_ids(lib):
     s, e, ntp = oracle.moe_align(cleaned, 8, 16)
     assert torch.equal(r.sorted_ids.cpu(), torch.from_numpy(s))
     assert int(r.num_tokens_padded.item()) == ntp
+
+
+@pytest.mark.parametrize("T,k", [(40, 4), (4, 8)])
+def test_align_validation_flags_bad_ids_any_size(lib, T, k):
+    ids, _ = workloads.draw_routing(T, 8, k, seed=5)
+    bad = ids.clone()
+    bad[1, 1] = 9
+    bad[2, 0] = -5
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    r = lib.moe_align(bad.to(DEV), 8, 16, validate=True, dev_err=err)
+    assert int(err.item()) & lib.DEVERR_BAD_EXPERT_ID
+    cleaned = bad.clone()
+    cleaned[1, 1] = -1
+    cleaned[2, 0] = -1
+    s, e, ntp = oracle.moe_align(cleaned, 8, 16)
+    assert torch.equal(r.sorted_ids.cpu(), torch.from_numpy(s))
+    assert torch.equal(r.expert_ids.cpu(), torch.from_numpy(e))
+    assert int(r.num_tokens_padded.item()) == ntp
+    # without validation nothing is flagged
+    err.zero_()
+    lib.moe_align(bad.to(DEV), 8, 16, validate=False, dev_err=err)
+    assert int(err.item()) == 0
 
 
 def test_align_runs_twice_identically(lib):

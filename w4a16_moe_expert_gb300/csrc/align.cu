@@ -178,6 +178,66 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
   if (ncta > 1) cluster.sync();  // peers may still be reading this CTA's counts
 }
 
+// The same routing for at most 32 slots (decode): warp 0 holds one slot per lane and sorts in
+// registers, the other warps clear the counters; after one barrier every thread fills the
+// sentinels and the unowned blocks past num_tokens_padded.  A slot's position is the padded
+// start of its expert (the sum of the padded counts of the smaller expert ids present) plus
+// its rank among the lower lanes holding the same id, so the order is the stable one.
+constexpr int kAlignSmallSlots = 32;
+
+__global__ void __launch_bounds__(kAlignThreads, 1)
+    moe_align_small_kernel(const int32_t* __restrict__ topk_ids, int n_slots, int E, int block_m,
+                           int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids,
+                           int32_t* __restrict__ ntp_out, int64_t capacity, int validate,
+                           int32_t* dev_err, int32_t* zero_words, int n_zero_words) {
+  __shared__ int32_t s_ntp;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int32_t sentinel = n_slots;
+  pdl_launch_dependents();  // the next kernel may start its prologue; it waits for our results
+  pdl_wait();               // topk_ids may come from the previous kernel in the stream
+  if (warp == 0) {
+    int e = lane < n_slots ? topk_ids[lane] : -1;
+    const bool bad = e < -1 || e >= E;
+    if (bad) e = -1;
+    if (validate && __any_sync(0xffffffffu, bad) && lane == 0)
+      set_dev_err(dev_err, W4A16_DEVERR_BAD_EXPERT_ID);
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const bool leader = e >= 0 && lane == __ffs(peers) - 1;
+    const int cnt = __popc(peers);
+    const int pad = leader ? (cnt + block_m - 1) / block_m * block_m : 0;
+    // padded start of this lane's expert, and the total
+    int start = 0, ntp = 0;
+    for (int j = 0; j < 32; ++j) {
+      const int ej = __shfl_sync(0xffffffffu, e, j);
+      const int pj = __shfl_sync(0xffffffffu, pad, j);
+      ntp += pj;
+      if (ej < e) start += pj;
+    }
+    if (e >= 0) {
+      const int pos = start + __popc(peers & ((1u << lane) - 1u));
+      if (pos < capacity) sorted_ids[pos] = lane;
+    }
+    if (leader) {
+      for (int p = start + cnt; p < start + pad; ++p)
+        if (p < capacity) sorted_ids[p] = sentinel;
+      for (int b = start / block_m; b < (start + pad) / block_m; ++b)
+        if (static_cast<int64_t>(b) * block_m < capacity) expert_ids[b] = e;
+    }
+    if (lane == 0) {
+      s_ntp = ntp;
+      *ntp_out = (ntp <= capacity) ? ntp : static_cast<int32_t>(capacity / block_m * block_m);
+      if (ntp > capacity) set_dev_err(dev_err, W4A16_DEVERR_CAPACITY);
+    }
+  } else {
+    for (int i = tid - 32; i < n_zero_words; i += kAlignThreads - 32) zero_words[i] = 0;
+  }
+  __syncthreads();
+  const int64_t ntp = s_ntp;
+  for (int64_t p = ntp + tid; p < capacity; p += kAlignThreads) sorted_ids[p] = sentinel;
+  const int64_t nblocks = capacity / block_m;
+  for (int64_t b = ntp / block_m + tid; b < nblocks; b += kAlignThreads) expert_ids[b] = -1;
+}
+
 // Activation rows in aligned order: out[p, :] = x[sorted_ids[p] / a_row_div, :] for every
 // routed position p < num_tokens_padded (padding rows are left as they are).  One warp per
 // row, 16-byte vectors; lets the GEMM stream activation tiles with 2-D TMA instead of gathering
@@ -245,6 +305,20 @@ cudaError_t launch_moe_align(const int32_t* topk_ids, int n_slots, int E, int bl
                              int32_t* sorted_ids, int32_t* expert_ids, int32_t* ntp,
                              int64_t capacity, int validate, int32_t* dev_err,
                              int32_t* zero_words, int n_zero_words, cudaStream_t stream) {
+  if (n_slots <= kAlignSmallSlots) {  // decode: one warp sorts in registers
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kAlignThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, moe_align_small_kernel, topk_ids, n_slots, E, block_m,
+                              sorted_ids, expert_ids, ntp, capacity, validate, dev_err,
+                              zero_words, n_zero_words);
+  }
   const size_t smem = align_smem_bytes(E);
   cudaError_t err = cudaFuncSetAttribute(moe_align_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
