@@ -71,7 +71,7 @@ def ulp_bf16(x: np.ndarray) -> np.ndarray:
 def test_float_to_bf16_matches_torch_rne():
     rng = np.random.default_rng(0)
     x = np.concatenate([
-        rng.standard_normal(200_000).astype(np.float32) * np.float32(10.0) ** rng.integers(-30, 30, 200_000),
+        (rng.standard_normal(200_000) * 10.0 ** rng.integers(-30, 30, 200_000)).astype(np.float32),
         rng.integers(0, 2 ** 32, 200_000, dtype=np.uint64).astype(np.uint32).view(np.float32),
         np.array([0.0, -0.0, np.inf, -np.inf, 3.3895314e38, 1e-40, -1e-45], np.float32),
     ])
