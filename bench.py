@@ -904,7 +904,8 @@ def run_profile_call(args):
     hint = max(1, round(T * wl.top_k / wl.E_global))
     ws = lib.gemm_workspace(T * wl.top_k, wl.E, W.N, W.K, bm, dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    kw = dict(workspace=ws, expected_rows_per_expert=hint, split_k=args.split, num_ctas=0)
+    kw = dict(workspace=ws, expected_rows_per_expert=hint, split_k=args.split, num_ctas=0,
+              cta_pairs=args.pairs)
     if args.profile_call == "gate_up":
         if bm >= 64:
             A, div = lib.gather_rows(x.to(dev), wl.top_k, r), 1
@@ -927,7 +928,8 @@ def run_profile_call(args):
     plan = lib.plan_gemm(n_slots, wl.E, W.N, W.K, bm, num_sms=torch.cuda.get_device_properties(
         dev).multi_processor_count, expected_rows_per_expert=hint)
     print(json.dumps({"profile_call": args.profile_call, "workload": wl.name, "T": T,
-                      "block_m": bm, "split_k_arg": args.split, "plan": plan,
+                      "block_m": bm, "split_k_arg": args.split, "cta_pairs_arg": args.pairs,
+                      "plan": plan,
                       "num_tokens_padded": int(r.num_tokens_padded.item()),
                       "launches": args.repeat}), flush=True)
 
@@ -953,6 +955,8 @@ def main():
                          "times, for an ncu capture; prints no bench line")
     ap.add_argument("--repeat", type=int, default=3)
     ap.add_argument("--split", type=int, default=0, help="--profile-call: fixed K split (0: planner)")
+    ap.add_argument("--pairs", type=int, default=0, choices=[0, 1, 2],
+                    help="--profile-call: 1 one CTA per tile, 2 CTA pairs (0: planner)")
     args = ap.parse_args()
     if args.profile_call:
         run_profile_call(args)

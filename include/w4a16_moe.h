@@ -165,12 +165,17 @@ w4a16_status_t w4a16_pack_weights_nvfp4(const uint8_t* codes, const uint8_t* sca
  * expected_rows_per_expert  host hint for the schedule (0: total_slots / E); it never
  *    changes results, which are independent of the schedule up to FP32 summation order
  *    (and bitwise identical between runs of the same schedule).
- * Schedule: unless `schedule` fixes split_k, the K split of a tile is picked on the device
- *    from *num_tokens_padded: when the routed (block, 128-row tile) units are fewer than half
- *    the CTAs, K is sliced (at most 8 slices of at least 1536 K elements) so that the units
- *    fill one wave; the slices' FP32 partials are summed in slice order by the last CTA to
- *    finish the tile (deterministic).  Without a workspace large enough for the partials
- *    tiles are never split.
+ * Schedule (picked per call unless `schedule` fixes it):
+ *    - 16- and 32-token blocks: the K split of a tile is picked on the device from
+ *      *num_tokens_padded.  When the routed (block, 128-row tile) units fill less than half
+ *      the CTAs every tile is sliced, otherwise only the tiles of a last, partial wave (at
+ *      most 8 slices of at least 1536 K elements each).  The slices' FP32 partials are summed
+ *      in slice order by the last CTA to finish the tile (deterministic).  Without a
+ *      workspace large enough for the partials tiles are never split.
+ *    - K <= 512 at 16- and 32-token blocks: 2 or 4 consecutive tiles of a block share one
+ *      work unit and its activation stages (tile groups).
+ *    - 128-token blocks of sorted rows with at most 4 tiles (N <= 512) and K >= 4096: CTA
+ *      pairs, one M = 256 MMA over the two CTAs of a cluster, each loading half the rows.
  * ---------------------------------------------------------------------------------------- */
 #define W4A16_EPILOGUE_NONE 0
 #define W4A16_EPILOGUE_SILU_MUL 1
@@ -363,6 +368,8 @@ typedef struct {
   int32_t num_ctas;
   int32_t stages;      /* weight/activation ring depth in shared memory */
   int32_t est_units;   /* estimated (block, tile, split) work units */
+  int32_t cta_pairs;   /* 2: CTA pairs (when the activation rows are sorted, as the layer's
+                          128-token blocks are), 1: one CTA per 128-row tile */
 } w4a16_plan_t;
 
 w4a16_status_t w4a16_plan_gemm(int total_slots, int E, int N, int K, int block_m,

@@ -90,6 +90,20 @@ def test_gemm_planner_grid_and_split():
         lib.plan_gemm(8, 128, 1536, 2000, 16, num_sms=148)
 
 
+def test_gemm_planner_cta_pairs():
+    # CTA pairs only for 128-token blocks whose rows are long (K >= 4096) and shared by at most
+    # four tiles: Kimi-K2 TP8 gate_up (N 512 = 4 tiles, K 7168) at T=8192
+    assert lib.plan_gemm(65536, 384, 512, 7168, 128, num_sms=148)["cta_pairs"] == 2
+    # its down projection (56 tiles, K 256), Qwen3 and Kimi-K2 EP8 prefill gate_up (12 and 32
+    # tiles), and decode blocks: one CTA per tile
+    assert lib.plan_gemm(65536, 384, 7168, 256, 128, num_sms=148)["cta_pairs"] == 1
+    assert lib.plan_gemm(32768, 128, 1536, 2048, 128, num_sms=148)["cta_pairs"] == 1
+    assert lib.plan_gemm(65536, 48, 4096, 7168, 128, num_sms=148)["cta_pairs"] == 1
+    assert lib.plan_gemm(256, 384, 512, 7168, 16, num_sms=148)["cta_pairs"] == 1
+    # short K at 128-token blocks: one CTA per tile
+    assert lib.plan_gemm(65536, 384, 512, 2048, 128, num_sms=148)["cta_pairs"] == 1
+
+
 def test_planner_rejects_bad_arguments(L):
     plan = lib.PlanDesc()
     assert L.w4a16_plan_gemm(8, 0, 128, 64, 16, 0, 148, ctypes.byref(plan)) == 1

@@ -75,7 +75,7 @@ class ScheduleDesc(ctypes.Structure):
 
 class PlanDesc(ctypes.Structure):
     _fields_ = [("block_m", ctypes.c_int32), ("split_k", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
-                ("stages", ctypes.c_int32), ("est_units", ctypes.c_int32)]
+                ("stages", ctypes.c_int32), ("est_units", ctypes.c_int32), ("cta_pairs", ctypes.c_int32)]
 
 
 _lib = None

@@ -239,8 +239,6 @@ struct GemmCall {
   bool one_kernel = false;  // an argument set of the single-kernel layer (one tile per unit)
 };
 
-// 128-token blocks use CTA pairs unless the schedule says otherwise.
-constexpr bool kPairsByDefault = false;
 
 // Checks a GEMM call and fills the kernel arguments and grid; *empty is set when there is
 // nothing to compute (no capacity or no experts).
@@ -352,7 +350,8 @@ static w4a16_status_t prepare_gemm(const GemmCall& c, const DeviceFacts& dev, Ge
   if (want_pair == 2 && !pair_ok)
     return fail(W4A16_INVALID_ARG, "CTA pairs need block_m 128, sorted activation rows, an even "
                                    "tile count and no K split");
-  a.pair = (want_pair == 2 || (want_pair == 0 && pair_ok && kPairsByDefault)) ? 1 : 0;
+  const bool pair_pays = pairs_pay(R->block_m, a.n_tiles, n_kb) && !c.one_kernel;
+  a.pair = (want_pair == 2 || (want_pair == 0 && pair_ok && pair_pays)) ? 1 : 0;
   if (a.pair) {  // whole-K tiles
     a.split_k = 1;
     a.split_auto = 0;

@@ -321,17 +321,6 @@ __device__ __forceinline__ void store_chunk16(const GemmArgs& a, const Unit& un,
   __syncwarp();  // the staging area is reused by the next chunk
 }
 
-// Waits in a pair kernel acquire at cluster scope (peers arrive on the even CTA's barriers).
-template <bool PAIR>
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                         int32_t* dev_err) {
-  return PAIR ? mbar_wait_cl(bar, parity, abort_flag, dev_err) : mbar_wait(bar, parity, abort_flag, dev_err);
-}
-template <bool PAIR>
-__device__ __forceinline__ bool wait_bar_plain(uint32_t bar, uint32_t parity) {
-  return PAIR ? mbar_wait_plain_cl(bar, parity) : mbar_wait_plain(bar, parity);
-}
-
 template <bool PAIR>
 __device__ __forceinline__ void mma_any(uint32_t d, uint32_t a_tmem, uint64_t bd, uint32_t idesc,
                                         uint32_t acc) {
@@ -393,8 +382,9 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       (reinterpret_cast<uintptr_t>(epi_rows + NT) + 15) & ~static_cast<uintptr_t>(15));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // CTA pairs: the even CTA of each two-CTA cluster issues the MMAs; the odd one forwards its
-  // activation tiles' arrival and its dequant / epilogue hand-offs to the even CTA's barriers
+  // CTA pairs: the even CTA of each two-CTA cluster issues the MMAs; the odd CTA's activation
+  // copies complete on the even CTA's barriers (cta_group::2 tensor copies) and its dequant and
+  // epilogue warps arrive there remotely
   const uint32_t crank = CL ? cluster_ctarank() : 0u;
   const bool leader = crank == 0;
   const int64_t unit0 = CL ? (blockIdx.x >> 1) : blockIdx.x;
@@ -410,7 +400,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       mbar_init(smem_u32(&wempty[s]), 4);
     }
     for (int s = 0; s < S_B; ++s) {
-      mbar_init(smem_u32(&bfull[s]), PAIR ? (leader ? 2 : 1) : ((FUSED || gather) ? kGatherThreads : 1));
+      mbar_init(smem_u32(&bfull[s]), PAIR ? 1 : ((FUSED || gather) ? kGatherThreads : 1));
       mbar_init(smem_u32(&bempty[s]), 1);
     }
     for (int s = 0; s < S_A; ++s) {
@@ -513,7 +503,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
         const int nsub = min(KS, un.kb1 - kb);
         const int s = it % S_W;
         const uint32_t ph = (it / S_W) & 1;
-        if (!__all_sync(0xffffffffu, wait_bar<PAIR>(smem_u32(&wempty[s]), ph ^ 1, abort_flag, a.dev_err)))
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&wempty[s]), ph ^ 1, abort_flag, a.dev_err)))
           goto wprod_done;
         if (lane == static_cast<int>(it & 31)) {
           const uint32_t wb = smem_u32(&wfull[s]);
@@ -561,7 +551,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
             const int nsub = min(KS, un.kb1 - kb);
             const int s = it % S_B;
             const uint32_t ph = (it / S_B) & 1;
-            if (!wait_bar<PAIR>(smem_u32(&bempty[s]), ph ^ 1, abort_flag, g.dev_err)) goto fprod_done;
+            if (!mbar_wait(smem_u32(&bempty[s]), ph ^ 1, abort_flag, g.dev_err)) goto fprod_done;
             const uint32_t bdst = smem_u32(b_ring + s * Cfg::kBBytes);
             for (int sb = 0; sb < nsub; ++sb) {
 #pragma unroll
@@ -579,7 +569,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
             const int nsub = min(KS, un.kb1 - kb);
             const int s = it % S_B;
             const uint32_t ph = (it / S_B) & 1;
-            if (!__all_sync(0xffffffffu, wait_bar<PAIR>(smem_u32(&bempty[s]), ph ^ 1, abort_flag, g.dev_err)))
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bempty[s]), ph ^ 1, abort_flag, g.dev_err)))
               goto fprod_done;
             const uint32_t bb = smem_u32(&bfull[s]);
             if (gt == 0)
@@ -620,7 +610,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
           const int nsub = min(KS, kb_end - kb);
           const int s = it % S_B;
           const uint32_t ph = (it / S_B) & 1;
-          if (!wait_bar<PAIR>(smem_u32(&bempty[s]), ph ^ 1, abort_flag, a.dev_err)) goto bprod_done;
+          if (!mbar_wait(smem_u32(&bempty[s]), ph ^ 1, abort_flag, a.dev_err)) goto bprod_done;
           const uint32_t bdst = smem_u32(b_ring + s * Cfg::kBBytes);
           // Padding rows are not loaded: MMA column j reads only B row j, so whatever a
           // padding row holds lands in a token column that the epilogue discards.
@@ -648,16 +638,19 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
           const int nsub = min(KS, kb_end - kb);
           const int s = it % S_B;
           const uint32_t ph = (it / S_B) & 1;
-          if (!__all_sync(0xffffffffu, wait_bar<PAIR>(smem_u32(&bempty[s]), ph ^ 1, abort_flag, a.dev_err)))
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bempty[s]), ph ^ 1, abort_flag, a.dev_err)))
             goto tprod_done;
-          const uint32_t bb = smem_u32(&bfull[s]);
-          if (lane == 0) mbar_arrive_expect_tx(bb, nsub * Cfg::kSubB);
+          // pairs: both CTAs' halves complete on the even CTA's barrier, which expects both
+          const uint32_t bb = PAIR ? mapa_shared(smem_u32(&bfull[s]), 0) : smem_u32(&bfull[s]);
+          if (lane == 0 && (!PAIR || leader))
+            mbar_arrive_expect_tx(smem_u32(&bfull[s]), (PAIR ? 2 : 1) * nsub * Cfg::kSubB);
           __syncwarp();
           for (int sb = 0; sb < nsub; ++sb) {
             if (lane != static_cast<int>((it * KS + sb) & 31)) continue;
             const uint32_t dst = smem_u32(b_ring + s * Cfg::kBBytes + sb * Cfg::kSubB);
-            tma_load_2d(dst, &a.tmap_a, (kb + sb) * kBlockK,
-                        static_cast<int>(un.b * a.block_m + (PAIR ? crank * (NT / 2) : 0)), bb);
+            const int y = static_cast<int>(un.b * a.block_m + (PAIR ? crank * (NT / 2) : 0));
+            if (PAIR) tma_load_2d_pair(dst, &a.tmap_a, (kb + sb) * kBlockK, y, bb);
+            else tma_load_2d(dst, &a.tmap_a, (kb + sb) * kBlockK, y, bb);
           }
           __syncwarp();
         }
@@ -673,23 +666,8 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
     constexpr uint32_t idesc = idesc_bf16_f32(PAIR ? 256 : 128, NT);
     const uint64_t b_desc0 = smem_desc_sw128(smem_u32(b_ring));
     if (PAIR && !leader) {
-      // odd CTA of a pair: pass each landed activation stage on to the even CTA's barrier,
-      // then wait for the pair's last MMAs before the TMEM they write is released
-      if (elect_one()) {
-        uint32_t it = 0;
-        for (int64_t u = CL ? unit0 : blockIdx.x; u < n_units; u += CL ? ustride : gridDim.x) {
-          const Unit un = decode_any<FUSED, CL>(a, a2, sm, units0_u, crank, u);
-          if (!un.ok) continue;
-          for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
-            const int sbi = it % S_B;
-            const uint32_t pb = (it / S_B) & 1;
-            if (!wait_bar<PAIR>(smem_u32(&bfull[sbi]), pb, abort_flag, a.dev_err)) goto fwd_done;
-            mbar_arrive_remote(mapa_shared(smem_u32(&bfull[sbi]), 0));
-          }
-        }
-      fwd_done:
-        wait_bar_plain<PAIR>(smem_u32(drain), 0);
-      }
+      // odd CTA of a pair: wait for the pair's last MMAs before the TMEM they write is released
+      if (elect_one()) mbar_wait_plain(smem_u32(drain), 0);
     } else if (elect_one()) {
       uint32_t it = 0, itb = 0, lu = 0;  // A ring, activation ring, accumulator positions
       constexpr int tpu = TPU;
@@ -699,7 +677,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
         const bool rows_gathered = FUSED ? !args_of<FUSED>(a, a2, un).a_sorted : gather;
         const int ab = lu & 1;
         const uint32_t pab = (lu >> 1) & 1;
-        if (!wait_bar<PAIR>(smem_u32(&accempty[ab]), pab ^ 1, abort_flag, a.dev_err)) goto mma_done;
+        if (!mbar_wait(smem_u32(&accempty[ab]), pab ^ 1, abort_flag, a.dev_err)) goto mma_done;
         tc_fence_after();
         // a tile group's tiles accumulate side by side: buffer ab holds tpu * NT columns
         const uint32_t d_tmem = tmem_base + ab * (NT * tpu);
@@ -719,9 +697,9 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
           const uint32_t pb = (jb / S_B) & 1;
           const int sa = it % S_A;
           const uint32_t pa = (it / S_A) & 1;
-          if (!wait_bar<PAIR>(smem_u32(&afull[sa]), pa, abort_flag, a.dev_err)) goto mma_done;
+          if (!mbar_wait(smem_u32(&afull[sa]), pa, abort_flag, a.dev_err)) goto mma_done;
           if (tg == 0) {
-            if (!wait_bar<PAIR>(smem_u32(&bfull[sbi]), pb, abort_flag, a.dev_err)) goto mma_done;
+            if (!mbar_wait(smem_u32(&bfull[sbi]), pb, abort_flag, a.dev_err)) goto mma_done;
             if (rows_gathered) fence_proxy_async_smem();  // cp.async (generic proxy) rows -> tensor core
           }
           tc_fence_after();
@@ -772,7 +750,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       }
     mma_done:
       commit_any<PAIR>(smem_u32(drain));
-      wait_bar_plain<PAIR>(smem_u32(drain), 0);
+      mbar_wait_plain(smem_u32(drain), 0);
     }
     __syncwarp();
   } else if (warp >= 4 && warp < 8) {
@@ -816,7 +794,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       named_bar_epi();
       const int ab = lu & 1;
       const uint32_t pab = (lu >> 1) & 1;
-      const bool ok = wait_bar<PAIR>(smem_u32(&accfull[ab]), pab, abort_flag, a.dev_err);
+      const bool ok = mbar_wait(smem_u32(&accfull[ab]), pab, abort_flag, a.dev_err);
       if (epi_any(!ok)) break;
       if (ids_ahead && u + gridDim.x < n_units) {
         ahead_u = u + gridDim.x;
@@ -967,7 +945,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
         const int sa = it % S_A;
         const uint32_t pa = (it / S_A) & 1;
         // warp-uniform decisions: tcgen05.st below is a warp-collective instruction
-        if (!__all_sync(0xffffffffu, wait_bar<PAIR>(smem_u32(&wfull[sw]), pw, abort_flag, a.dev_err)))
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&wfull[sw]), pw, abort_flag, a.dev_err)))
           goto dq_done;
         uint4 lo[KS], hi[KS];
         uint32_t s2[KS];
@@ -982,7 +960,7 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
         }
         __syncwarp();  // every lane holds its rows: the weight stage may be refilled
         if (lane == 0) mbar_arrive(smem_u32(&wempty[sw]));
-        if (!__all_sync(0xffffffffu, wait_bar<PAIR>(smem_u32(&aempty[sa]), pa ^ 1, abort_flag, a.dev_err)))
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&aempty[sa]), pa ^ 1, abort_flag, a.dev_err)))
           goto dq_done;
         tc_fence_after();
         if (nvfp4) {
@@ -1026,10 +1004,10 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
     // give in-flight copies a bounded chance to land before the CTA's memory goes away
     const uint32_t nw = *w_issued, nb = *b_issued;
     for (uint32_t j = (nw > static_cast<uint32_t>(S_W) ? nw - S_W : 0); j < nw; ++j)
-      wait_bar_plain<PAIR>(smem_u32(&wfull[j % S_W]), (j / S_W) & 1);
-    if (any_tma)
+      mbar_wait_plain(smem_u32(&wfull[j % S_W]), (j / S_W) & 1);
+    if (any_tma && (!PAIR || leader))  // a pair's activation loads complete on the even CTA
       for (uint32_t j = (nb > static_cast<uint32_t>(S_B) ? nb - S_B : 0); j < nb; ++j)
-        wait_bar_plain<PAIR>(smem_u32(&bfull[j % S_B]), (j / S_B) & 1);
+        mbar_wait_plain(smem_u32(&bfull[j % S_B]), (j / S_B) & 1);
   }
   tc_fence_before();
   __syncthreads();
@@ -1121,6 +1099,7 @@ void plan_gemm(int total_slots, int E, int N, int K, int block_m, int rows_per_e
   plan->num_ctas = (split_max > 1 && few) ? num_sms
                                           : std::max(1, std::min(num_sms, plan->est_units));
   plan->stages = stages_for_block_m(block_m);
+  plan->cta_pairs = pairs_pay(block_m, n_tiles, n_kb) ? 2 : 1;
 }
 
 // cuTensorMapEncodeTiled from the driver (fetched once; no link-time libcuda dependency).

@@ -85,6 +85,18 @@ constexpr int tile_group_max(int block_m) { return block_m <= 16 ? 4 : (block_m 
 // K blocks (64 wide) of a unit short enough for tile groups: at most two pipeline stages.
 constexpr int kGroupMaxKb = 8;
 
+// CTA pairs by default where a 128-token block's activation rows are long and shared by few
+// tiles (N <= 512, K >= 4096): each tile of a block re-reads the block's rows, and a pair reads
+// half of them per CTA.  Measured on GB300 (single flushed calls, one CTA per tile against
+// pairs): Kimi-K2 TP8 gate_up at T=8192 (4 tiles, K = 7168) 496.3 -> 480.9 us, Zipf routing
+// 482.0 -> 459.5; where blocks have 12-56 tiles pairs were 0-5% slower (Qwen3 T=4096 gate_up
+// 172.7 -> 176.8, Kimi-K2 EP8 T=16384 gate_up 678.5 -> 697.0, TP8 down 705.2 -> 737.9).
+constexpr int kPairMaxTiles = 4;
+constexpr int kPairMinKb = 64;
+inline bool pairs_pay(int block_m, int n_tiles, int n_kb) {
+  return block_m == 128 && n_tiles % 2 == 0 && n_tiles <= kPairMaxTiles && n_kb >= kPairMinKb;
+}
+
 // The fused layer call: gate_up (a) then down (a2) in one cooperative persistent launch.
 cudaError_t launch_layer_fused(GemmArgs& a, GemmArgs& a2, int grid, cudaStream_t stream);
 
