@@ -64,12 +64,13 @@ DECODE_ROOFLINE_T = 64
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum from an ncu capture of
 # that launch), valid only while the GEMM kernel's sources hash to the recorded value.
 # Captured with `bench.py --profile-call <proj> --workload qwen3_30b_a3b --tokens <T> --repeat 3`
-# under `ncu --set full -k regex:moe_gemm -s 2 -c 1` (L2 flushed before each call).
-_SRC_SHA = "61b2093d6eeddb2a6f1c8e56997c6c4c12a2b04c076f4e033ba4c81939a814cc"
+# under `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,... -k regex:moe_gemm -s 2 -c 1`
+# (L2 flushed before each call).
+_SRC_SHA = "5daef033e52cc675625578d32e6fda3a6fc4275726afe022a09586d9ca15028d"
 ROOFLINE_TRAFFIC = {
-    "gate_up_T4096": {"bytes": 392441088 + 52274176, "sources_sha256": _SRC_SHA},
-    "down_T4096": {"bytes": 175614976 + 217982464, "sources_sha256": _SRC_SHA},
-    "gate_up_T64": {"bytes": 223302400 + 3735296, "sources_sha256": _SRC_SHA},
+    "gate_up_T4096": {"bytes": 392447488 + 52334848, "sources_sha256": _SRC_SHA},
+    "down_T4096": {"bytes": 175636736 + 218036480, "sources_sha256": _SRC_SHA},
+    "gate_up_T64": {"bytes": 223302400 + 3445248, "sources_sha256": _SRC_SHA},
 }
 GEMM_SOURCES = ("w4a16_moe_expert_gb300/csrc/gemm.cu", "w4a16_moe_expert_gb300/csrc/gemm.cuh",
                 "w4a16_moe_expert_gb300/csrc/common.cuh")
