@@ -141,3 +141,24 @@ def test_pairs_rejected_where_they_cannot_run(lib, mode):
     xs = lib.gather_rows(x.to(DEV), 2, r)
     with pytest.raises(lib.LibraryError, match="invalid argument"):
         lib.moe_gemm(xs, 1, W, r, row_flags=lib.A_ROWS_SORTED, cta_pairs=mode, split_k=2)
+
+
+def test_planner_default_pairs_long_k_few_tiles(lib):
+    """128-token blocks with 4 tiles (N 512) and K 4096: the planner's default is the pair
+    schedule.  Its rows match the oracle and, bit for bit, the explicit pair and one-CTA
+    schedules (results never depend on the schedule)."""
+    T, k, E, N, K = 240, 4, 6, 512, 4096
+    assert lib.plan_gemm(T * k, E, N, K, 128, num_sms=148)["cta_pairs"] == 2
+    qw, sc, x, ids, W, r, xs, (s, e, ntp) = _case(lib, T, k, E, N, K, 58, True)
+    kw = dict(epilogue=1, row_flags=lib.A_ROWS_SORTED)
+    dflt = lib.moe_gemm(xs, 1, W, r, **kw).cpu()
+    two = lib.moe_gemm(xs, 1, W, r, cta_pairs=2, **kw).cpu()
+    one = lib.moe_gemm(xs, 1, W, r, cta_pairs=1, **kw).cpu()
+    rows = routed_rows(ids)
+    assert torch.equal(bits(dflt[rows]), bits(two[rows]))
+    assert torch.equal(bits(dflt[rows]), bits(one[rows]))
+    sample = rows[::7]
+    ref = oracle.silu_mul(oracle.gemm_rows(x, k, qw, sc, sample.numpy(),
+                                           ids.reshape(-1)[sample].numpy().astype("int64"),
+                                           out_f32=True))
+    assert_close_bf16(dflt[sample], ref, "planner-default pairs, K 4096")
