@@ -239,7 +239,6 @@ struct GemmCall {
   bool one_kernel = false;  // an argument set of the single-kernel layer (one tile per unit)
 };
 
-
 // Checks a GEMM call and fills the kernel arguments and grid; *empty is set when there is
 // nothing to compute (no capacity or no experts).
 static w4a16_status_t prepare_gemm(const GemmCall& c, const DeviceFacts& dev, GemmArgs* out,
