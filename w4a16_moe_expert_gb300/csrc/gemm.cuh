@@ -8,7 +8,8 @@
 namespace w4a16 {
 
 struct GemmArgs {
-  CUtensorMap tmap_a;  // activations: box 64 x 1 (row gather) or 64 x block_m (sorted rows)
+  CUtensorMap tmap_a;   // sorted rows, box 64 x block_m (single-kernel layer)
+  CUtensorMap tmap_a3;  // sorted rows as [K / 64][rows][64], box 64 x rows x (K blocks a stage)
   const uint16_t* A;
   int64_t lda;
   int a_row_div;
