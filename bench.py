@@ -66,11 +66,11 @@ DECODE_ROOFLINE_T = 64
 # Captured with `bench.py --profile-call <proj> --workload qwen3_30b_a3b --tokens <T> --repeat 3`
 # under `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,... -k regex:moe_gemm -s 2 -c 1`
 # (L2 flushed before each call).
-_SRC_SHA = "8610329448960426481ec8e136b2874f670657c5be739f174b84819753bfffc1"
+_SRC_SHA = "d9e7e266b5e73c2684a94ea93bd7f76ddfb14db105ad2350bdb7f17d32f03222"
 ROOFLINE_TRAFFIC = {
-    "gate_up_T4096": {"bytes": 392439808 + 52040960, "sources_sha256": _SRC_SHA},
-    "down_T4096": {"bytes": 175636224 + 218135040, "sources_sha256": _SRC_SHA},
-    "gate_up_T64": {"bytes": 223310336 + 3528448, "sources_sha256": _SRC_SHA},
+    "gate_up_T4096": {"bytes": 392477440 + 52742400, "sources_sha256": _SRC_SHA},
+    "down_T4096": {"bytes": 175636480 + 218062848, "sources_sha256": _SRC_SHA},
+    "gate_up_T64": {"bytes": 223313664 + 3650304, "sources_sha256": _SRC_SHA},
 }
 GEMM_SOURCES = ("w4a16_moe_expert_gb300/csrc/gemm.cu", "w4a16_moe_expert_gb300/csrc/gemm.cuh",
                 "w4a16_moe_expert_gb300/csrc/common.cuh")

@@ -541,11 +541,16 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
           fence_proxy_async_global();
         }
         if (!g.a_sorted) {
-          int32_t arow[R];
+          const uint16_t* srow[R];  // as in the plain kernel's gather: per-row source, swizzled offset
+          uint32_t doff[R];
 #pragma unroll
           for (int j = 0; j < R; ++j) {
             const int32_t i = __ldg(g.sorted_ids + static_cast<int64_t>(un.b) * g.block_m + (gt >> 3) + 8 * j);
-            arow[j] = (i >= 0 && i < g.total_slots) ? i / g.a_row_div : -1;
+            const int r = (gt >> 3) + 8 * j;
+            srow[j] = (i >= 0 && i < g.total_slots)
+                          ? g.A + static_cast<int64_t>(i / g.a_row_div) * g.lda + c * 8
+                          : nullptr;
+            doff[j] = static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
           }
           for (int kb = un.kb0; kb < un.kb1; kb += KS, ++it) {
             const int nsub = min(KS, un.kb1 - kb);
@@ -554,13 +559,11 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
             if (!mbar_wait(smem_u32(&bempty[s]), ph ^ 1, abort_flag, g.dev_err)) goto fprod_done;
             const uint32_t bdst = smem_u32(b_ring + s * Cfg::kBBytes);
             for (int sb = 0; sb < nsub; ++sb) {
+              const uint32_t sdst = bdst + sb * Cfg::kSubB;
+              const int koff = (kb + sb) * kBlockK;
 #pragma unroll
-              for (int j = 0; j < R; ++j) {
-                if (arow[j] < 0) continue;
-                const int r = (gt >> 3) + 8 * j;
-                const uint32_t dst = bdst + sb * Cfg::kSubB + r * 128 + ((c ^ (r & 7)) << 4);
-                cp_async_16(dst, g.A + static_cast<int64_t>(arow[j]) * g.lda + (kb + sb) * kBlockK + c * 8, 16u);
-              }
+              for (int j = 0; j < R; ++j)
+                if (srow[j]) cp_async_16(sdst + doff[j], srow[j] + koff, 16u);
             }
             cp_async_arrive_noinc(smem_u32(&bfull[s]));
           }
@@ -598,11 +601,18 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
       for (int64_t u = CL ? unit0 : blockIdx.x; u < n_units; u += CL ? ustride : gridDim.x) {
         const Unit un = decode_any<FUSED, CL>(a, a2, sm, units0_u, crank, u);
         if (!un.ok) continue;
-        int32_t arow[R];
+        // per row of this thread: its source (chunk c of the row, K block 0) and its swizzled
+        // destination offset within a sub-block; null source for padding rows
+        const uint16_t* srow[R];
+        uint32_t doff[R];
 #pragma unroll
         for (int j = 0; j < R; ++j) {
           const int32_t i = __ldg(a.sorted_ids + static_cast<int64_t>(un.b) * a.block_m + (g >> 3) + 8 * j);
-          arow[j] = (i >= 0 && i < a.total_slots) ? i / a.a_row_div : -1;
+          const int r = (g >> 3) + 8 * j;
+          srow[j] = (i >= 0 && i < a.total_slots)
+                        ? a.A + static_cast<int64_t>(i / a.a_row_div) * a.lda + c * 8
+                        : nullptr;
+          doff[j] = static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
         }
         // a tile group's tiles share the block's activation stages: they are loaded once
         const int kb_end = TPU > 1 ? a.n_kb : un.kb1;
@@ -615,13 +625,11 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
           // Padding rows are not loaded: MMA column j reads only B row j, so whatever a
           // padding row holds lands in a token column that the epilogue discards.
           for (int sb = 0; sb < nsub; ++sb) {
+            const uint32_t sdst = bdst + sb * Cfg::kSubB;
+            const int koff = (kb + sb) * kBlockK;
 #pragma unroll
-            for (int j = 0; j < R; ++j) {
-              if (arow[j] < 0) continue;
-              const int r = (g >> 3) + 8 * j;
-              const uint32_t dst = bdst + sb * Cfg::kSubB + r * 128 + ((c ^ (r & 7)) << 4);
-              cp_async_16(dst, a.A + static_cast<int64_t>(arow[j]) * a.lda + (kb + sb) * kBlockK + c * 8, 16u);
-            }
+            for (int j = 0; j < R; ++j)
+              if (srow[j]) cp_async_16(sdst + doff[j], srow[j] + koff, 16u);
           }
           cp_async_arrive_noinc(smem_u32(&bfull[s]));
         }
