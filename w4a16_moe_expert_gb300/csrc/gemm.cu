@@ -541,7 +541,9 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
           fence_proxy_async_global();
         }
         if (!g.a_sorted) {
-          const uint16_t* srow[R];  // as in the plain kernel's gather: per-row source, swizzled offset
+          // per row of this thread: its source (chunk c, K block 0), null for a padding row,
+          // and its swizzled destination offset within a sub-block
+          const uint16_t* srow[R];
           uint32_t doff[R];
 #pragma unroll
           for (int j = 0; j < R; ++j) {
@@ -637,22 +639,21 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
     bprod_done:
       cp_async_wait_all();
     } else if (warp == 2) {
-      // rows already in sorted order: one 2-D TMA tile per K sub-block, rotating lanes
+      // rows already in sorted order: one 3-D tensor copy per stage, issued by a lane that
+      // rotates over the warp
       for (int64_t u = CL ? unit0 : blockIdx.x; u < n_units; u += CL ? ustride : gridDim.x) {
         const Unit un = decode_any<FUSED, CL>(a, a2, sm, units0_u, crank, u);
         if (!un.ok) continue;
         const int kb_end = TPU > 1 ? a.n_kb : un.kb1;  // tile groups: loaded once
         for (int kb = un.kb0; kb < kb_end; kb += KS, ++it) {
-          const int nsub = min(KS, kb_end - kb);
           const int s = it % S_B;
           const uint32_t ph = (it / S_B) & 1;
           if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bempty[s]), ph ^ 1, abort_flag, a.dev_err)))
             goto tprod_done;
           // pairs: both CTAs' halves complete on the even CTA's barrier, which expects both
           const uint32_t bb = PAIR ? mapa_shared(smem_u32(&bfull[s]), 0) : smem_u32(&bfull[s]);
-          // one 3-D copy per stage: KS blocks of 64 K (blocks past K are zero-filled and still
-          // counted, so a stage always expects the whole box)
-          (void)nsub;
+          // the copy always moves KS blocks of 64 K: in a short last stage the blocks past K are
+          // zero-filled (and still counted), those past a K slice's end are loaded and unused
           if (lane == 0 && (!PAIR || leader))
             mbar_arrive_expect_tx(smem_u32(&bfull[s]), (PAIR ? 2 : 1) * KS * Cfg::kSubB);
           __syncwarp();
