@@ -66,11 +66,11 @@ DECODE_ROOFLINE_T = 64
 # Captured with `bench.py --profile-call <proj> --workload qwen3_30b_a3b --tokens <T> --repeat 3`
 # under `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,... -k regex:moe_gemm -s 2 -c 1`
 # (L2 flushed before each call).
-_SRC_SHA = "c3470f0e46def72c65a2886e05e2f5465bdf2576c197dca0c3b20ec1b9543ca3"
+_SRC_SHA = "e62345994abfe2407b69385d248fc535e29f7e6956f7553b821b9328f1057d03"
 ROOFLINE_TRAFFIC = {
-    "gate_up_T4096": {"bytes": 392439552 + 52169728, "sources_sha256": _SRC_SHA},
-    "down_T4096": {"bytes": 175635456 + 218219008, "sources_sha256": _SRC_SHA},
-    "gate_up_T64": {"bytes": 223311104 + 3504384, "sources_sha256": _SRC_SHA},
+    "gate_up_T4096": {"bytes": 392437760 + 52313600, "sources_sha256": _SRC_SHA},
+    "down_T4096": {"bytes": 175649280 + 218104576, "sources_sha256": _SRC_SHA},
+    "gate_up_T64": {"bytes": 223310336 + 3434752, "sources_sha256": _SRC_SHA},
 }
 GEMM_SOURCES = ("w4a16_moe_expert_gb300/csrc/gemm.cu", "w4a16_moe_expert_gb300/csrc/gemm.cuh",
                 "w4a16_moe_expert_gb300/csrc/common.cuh")

@@ -958,6 +958,39 @@ __device__ __forceinline__ void gemm_body(const GemmArgs& a, const GemmArgs& a2)
         // warp-uniform decisions: tcgen05.st below is a warp-collective instruction
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&wfull[sw]), pw, abort_flag, a.dev_err)))
           goto dq_done;
+        if (TPU > 1 && scaled && !nvfp4) {
+          // tile groups (one stage per tile): block 0 is converted while the A slot is still
+          // busy, the other blocks' codes are read after it frees (the weight stage is released
+          // after them).  Measured on GB300: Kimi-K2 TP8 down at T=1024 (32-token blocks,
+          // groups of 2) 142.0 -> 131.7 us; without groups it gained nothing and cost up to
+          // 2 us at 16-token gate_up calls.
+          const uint8_t* wst = w_ring + sw * Cfg::kWBytes;
+          uint32_t v0[32];
+          dequant_row64_scaled(reinterpret_cast<const uint4*>(wst)[t],
+                               reinterpret_cast<const uint4*>(wst + kCodeHalfBytes)[t],
+                               reinterpret_cast<const uint32_t*>(wst + kScaleOffset)[t], v0);
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&aempty[sa]), pa ^ 1, abort_flag, a.dev_err)))
+            goto dq_done;
+          tc_fence_after();
+          tmem_st32(lane_base + sa * (KS * 32), v0);
+#pragma unroll
+          for (int sb = 1; sb < KS; ++sb) {
+            if (sb < nsub) {
+              const uint8_t* ch = wst + sb * kChunkBytes;
+              uint32_t v[32];
+              dequant_row64_scaled(reinterpret_cast<const uint4*>(ch)[t],
+                                   reinterpret_cast<const uint4*>(ch + kCodeHalfBytes)[t],
+                                   reinterpret_cast<const uint32_t*>(ch + kScaleOffset)[t], v);
+              tmem_st32(lane_base + sa * (KS * 32) + sb * 32, v);
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&wempty[sw]));
+          tmem_wait_st();
+          tc_fence_before();
+          arrive_handoff<PAIR>(smem_u32(&afull[sa]), leader, lane);
+          continue;
+        }
         uint4 lo[KS], hi[KS];
         uint32_t s2[KS];
 #pragma unroll
