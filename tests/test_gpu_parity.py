@@ -330,6 +330,23 @@ def test_gemm_fp32_output_mode(lib):
     assert torch.equal(bits(C.to(torch.bfloat16)), bits(lib.moe_gemm(x.to(DEV), 4, W, r)))
 
 
+@pytest.mark.parametrize("bm", [16, 128])
+@pytest.mark.parametrize("K", [64, 128, 192, 320])
+def test_sorted_rows_shorter_than_a_stage(lib, bm, K):
+    # sorted activation rows come as one tensor copy per pipeline stage (4 K blocks of 64 at
+    # 16-token blocks, 2 at 128-token blocks); K shorter than a stage, or a short last stage,
+    # makes the copy reach past K (those blocks are zero-filled and not multiplied)
+    T, k, E, N = 48, 4, 6, 256
+    qw, sc, x, ids, W, r, (s, e, ntp) = _gemm_case(lib, T, k, E, N, K, bm, 70 + K)
+    xs = lib.gather_rows(x.to(DEV), k, r)
+    C = lib.moe_gemm(xs, 1, W, r, row_flags=lib.A_ROWS_SORTED | lib.C_FP32).cpu()
+    ref = oracle.moe_gemm(x, k, qw, sc, s, e, ntp, bm, T * k, out_f32=True)
+    rows = routed_rows(ids)
+    g, rf = C[rows], ref[rows]
+    rms = float(rf.pow(2).mean().sqrt())
+    assert float((g - rf).abs().max()) <= 1e-3 * rms, f"bm {bm}, K {K}"  # FP32 sums
+
+
 # ---- top-k sum and the whole layer --------------------------------------------------------------
 
 def test_topk_sum_parity(lib):
