@@ -347,6 +347,23 @@ def test_sorted_rows_shorter_than_a_stage(lib, bm, K):
     assert float((g - rf).abs().max()) <= 1e-3 * rms, f"bm {bm}, K {K}"  # FP32 sums
 
 
+@pytest.mark.parametrize("split", [2, 3, 5])
+def test_sorted_rows_with_k_slices(lib, split):
+    # K = 768 (12 blocks, three 4-block stages) cut into slices that end inside a stage: the
+    # stage's copy loads blocks past the slice end, which the slice must not multiply
+    T, k, E, N, K = 40, 4, 6, 256, 768
+    qw, sc, x, ids, W, r, (s, e, ntp) = _gemm_case(lib, T, k, E, N, K, 16, 80 + split)
+    xs = lib.gather_rows(x.to(DEV), k, r)
+    flags = lib.A_ROWS_SORTED | lib.C_FP32
+    whole = lib.moe_gemm(xs, 1, W, r, row_flags=flags, split_k=1).cpu()
+    sliced = lib.moe_gemm(xs, 1, W, r, row_flags=flags, split_k=split).cpu()
+    ref = oracle.moe_gemm(x, k, qw, sc, s, e, ntp, 16, T * k, out_f32=True)
+    rows = routed_rows(ids)
+    rms = float(ref[rows].pow(2).mean().sqrt())
+    assert float((sliced[rows] - ref[rows]).abs().max()) <= 1e-3 * rms, f"split {split}"
+    assert float((sliced[rows] - whole[rows]).abs().max()) <= 1e-3 * rms  # FP32 sums, other order
+
+
 # ---- top-k sum and the whole layer --------------------------------------------------------------
 
 def test_topk_sum_parity(lib):
